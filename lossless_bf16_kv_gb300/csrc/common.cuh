@@ -1,0 +1,126 @@
+// common.cuh -- device helpers shared by the SplitZip kernels (sm_103a).
+//
+// Nothing here is arithmetic of the codec itself: it is the workspace layout,
+// the tile-state word of the cross-tile escape prefix, PTX wrappers and a
+// multiply-shift division by the chunk size.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace splitzip {
+
+constexpr int kThreads = 256;  // every kernel runs 256-thread CTAs (8 warps)
+constexpr int kWarps = kThreads / 32;
+
+// ----------------------------------------------------------- workspace
+//
+// [0, 4096)      header (below)
+// [4096, ...)    one 64-bit tile-state word per encode tile
+struct WsHeader {
+    uint32_t ticket;        // encode: next tile id handed to a starting CTA
+    uint32_t done;          // encode: CTAs finished in the running launch
+    uint32_t epoch;         // encode: launch counter, tags tile-state words
+    uint32_t status;        // encode: status bits raised by the running launch
+    uint32_t last_status;   // encode: status bits of the last finished launch
+    uint32_t cal_done;      // calibrate: CTAs finished in the running launch
+    uint64_t last_escapes;  // encode: E of the last finished launch
+    uint64_t cal_covered;   // calibrate: covered count (synchronous API readback)
+    uint8_t cal_cb[16];     // calibrate: codebook (synchronous API readback)
+    uint64_t reserved[24];
+    unsigned long long hist[256];  // calibrate: global exponent histogram, zero between launches
+};
+static_assert(sizeof(WsHeader) <= 4096, "header must fit its slot");
+constexpr size_t kWsHeaderBytes = 4096;
+
+constexpr uint32_t kStatusOverflow = 1u;
+constexpr uint32_t kStatusTimeout = 2u;
+
+// Tile-state word of the decoupled look-back:
+//   bits  0..31  value (aggregate or inclusive prefix of escape counts)
+//   bits 32..33  flag: 0 not ready, 1 aggregate, 2 inclusive prefix
+//   bits 34..63  epoch tag (launch counter mod 2^30); a word with another tag
+//                is left over from an earlier launch and reads as not ready.
+constexpr uint32_t kFlagAggregate = 1u;
+constexpr uint32_t kFlagPrefix = 2u;
+
+__host__ __device__ __forceinline__ uint64_t make_state(uint32_t flag, uint32_t value,
+                                                        uint32_t epoch) {
+    return (uint64_t)value | ((uint64_t)flag << 32) | ((uint64_t)(epoch & 0x3FFFFFFFu) << 34);
+}
+__device__ __forceinline__ uint32_t state_flag(uint64_t w, uint32_t epoch) {
+    if ((uint32_t)(w >> 34) != (epoch & 0x3FFFFFFFu)) return 0;
+    return (uint32_t)(w >> 32) & 3u;
+}
+
+// ------------------------------------------------------------- PTX bits
+
+// prmt.b32 in its default mode: selector nibble bit 3 replicates the sign bit
+// of the selected byte (used by the decode's 16-entry codebook lookup).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Streaming loads (read once: evict-first).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.cs.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_stream4(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.cs.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+// Streaming stores (written once, not re-read by this kernel).
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_stream8(void* p, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ------------------------------------------------------------- division
+//
+// q = floor(x / d) as (x * m) >> 33 with m = ceil(2^33 / d), exact for
+// x < 2^17 and 1 <= d <= 2^16 (Granlund & Montgomery, "Division by Invariant
+// Integers using Multiplication", 1994): with m*d = 2^33 + e, 0 <= e < d, the
+// error term x*e / (d * 2^33) stays below 1/d because x*e < 2^17 * 2^16.
+struct ChunkDiv {
+    uint32_t d;  // chunk size
+    uint32_t m;  // ceil(2^33 / d)
+};
+__host__ __device__ __forceinline__ ChunkDiv make_chunk_div(uint32_t d) {
+    ChunkDiv c;
+    c.d = d;
+    c.m = (uint32_t)(((1ull << 33) + d - 1) / d);
+    return c;
+}
+__device__ __forceinline__ uint32_t chunk_quot(ChunkDiv c, uint32_t x) {
+    return (uint32_t)(((uint64_t)x * c.m) >> 33);
+}
+
+}  // namespace splitzip

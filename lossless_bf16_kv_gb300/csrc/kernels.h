@@ -1,0 +1,65 @@
+// kernels.h -- launch arguments and launchers of the SplitZip kernels
+// (internal to the library; the public interface is include/splitzip.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace splitzip {
+
+constexpr uint32_t kTestStallFirstTile = 1u;    // tile 0 never publishes (test hook)
+constexpr uint32_t kStatusBadWorkspace = 4u;    // a CTA drew a ticket past the grid
+constexpr uint32_t kDefaultSpinLimit = 1u << 23;  // polls of >= 100 ns: about a second
+
+struct EncodeArgs {
+    const uint8_t* x;  // input bit patterns, 16-byte aligned
+    uint32_t n;        // elements
+    ChunkDiv cdiv;     // chunk size and its division multiplier
+    uint32_t nchunks;  // ceil(n / chunk)
+    uint8_t* codes;
+    uint8_t* signman;
+    uint16_t* esc_pos;
+    uint8_t* esc_val;
+    uint32_t* chunk_off;
+    uint64_t esc_capacity;
+    uint8_t* ws;         // workspace: header + tile states
+    uint32_t num_tiles;  // grid size
+    uint32_t spin_limit;
+    uint32_t test_flags;
+    uint32_t cbw[4];     // codebook bytes, 4 per word, little-endian
+};
+
+struct DecodeArgs {
+    const uint8_t* codes;
+    const uint8_t* signman;
+    const uint16_t* esc_pos;
+    const uint8_t* esc_val;
+    const uint32_t* chunk_off;
+    uint64_t esc_count;  // escape entries present
+    uint32_t n;
+    ChunkDiv cdiv;
+    uint32_t nchunks;
+    uint8_t* y;          // output bit patterns, 16-byte aligned
+    uint32_t num_tiles;
+    uint32_t cbw[4];
+};
+
+struct CalibArgs {
+    const uint8_t* x;
+    uint32_t n;
+    uint32_t grid;
+    uint8_t* ws;
+    uint8_t* cb_out;        // 16 bytes, device
+    uint64_t* covered_out;  // device
+};
+
+int encode_tile_elems(bool e5m2);
+int decode_tile_elems(bool e5m2);
+cudaError_t launch_encode(const EncodeArgs& a, bool e5m2, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, bool e5m2, cudaStream_t s);
+cudaError_t launch_calibrate(const CalibArgs& a, bool e5m2, cudaStream_t s);
+uint32_t calibrate_grid(uint32_t n, int num_sms);
+
+}  // namespace splitzip
