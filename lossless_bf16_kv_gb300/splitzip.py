@@ -1,0 +1,336 @@
+"""Thin Python binding of the SplitZip C ABI (include/splitzip.h).
+
+Argument marshalling only: PyTorch supplies device memory and streams, and
+every step of the codec runs in the library's CUDA kernels.  The binding fails
+loudly if the library is missing; there is no CPU fallback.
+
+Low level: ``splitzip_*`` functions with the C names, taking torch tensors.
+High level: ``ChunkLocalSplitZipGPU``, shaped like the codec API the pages
+describe ("SplitZip: Ultra-Fast Lossless KV Compression for Disaggregated LLM
+Serving", README section Codec API: ``calibrate(x) -> coverage``,
+``encode(x) -> encoded`` with ``.compressed_bytes``, ``decode(encoded)``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIBPATH = os.path.join(_PKG, "_lib", "libsplitzip.so")
+
+OK, ERR_INVALID_ARG, ERR_ESCAPE_OVERFLOW, ERR_TIMEOUT, ERR_CUDA, ERR_WORKSPACE = range(6)
+STATUS_NAMES = {OK: "OK", ERR_INVALID_ARG: "INVALID_ARG", ERR_ESCAPE_OVERFLOW: "ESCAPE_OVERFLOW",
+                ERR_TIMEOUT: "TIMEOUT", ERR_CUDA: "CUDA", ERR_WORKSPACE: "WORKSPACE"}
+MAX_CHUNK = 65536
+MAX_ELEMENTS = 0xFFFFFFFF
+TEST_STALL_FIRST_TILE = 0x1
+
+
+class SplitZipError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class Codebook(ctypes.Structure):
+    _fields_ = [("exp", ctypes.c_uint8 * 16)]
+
+
+class Streams(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("signman", ctypes.c_void_p),
+                ("esc_pos", ctypes.c_void_p), ("esc_val", ctypes.c_void_p),
+                ("chunk_off", ctypes.c_void_p), ("esc_capacity", ctypes.c_uint64)]
+
+
+class EncodeTestOpts(ctypes.Structure):
+    _fields_ = [("spin_limit", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libsplitzip.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBPATH):
+        raise ImportError(f"{LIBPATH} is missing: build it first "
+                          "(python -m lossless_bf16_kv_gb300._build)")
+    lib = ctypes.CDLL(LIBPATH)
+    vp, u64, u32, i32, st = (ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int,
+                             ctypes.c_int)
+    cbp, sp = ctypes.POINTER(Codebook), ctypes.POINTER(Streams)
+    sig = {
+        "splitzip_workspace_bytes": (ctypes.c_size_t, [u64, u32]),
+        "splitzip_workspace_init": (st, [vp, ctypes.c_size_t, vp]),
+        "splitzip_codes_bytes": (u64, [u64]),
+        "splitzip_signman_bytes": (u64, [u64]),
+        "splitzip_signman_bytes_e5m2": (u64, [u64]),
+        "splitzip_num_chunks": (u64, [u64, u32]),
+        "splitzip_compressed_bytes": (u64, [u64, u32, u64]),
+        "splitzip_compressed_bytes_e5m2": (u64, [u64, u32, u64]),
+        "splitzip_calibrate": (st, [vp, u64, cbp, ctypes.POINTER(ctypes.c_double), vp, vp]),
+        "splitzip_calibrate_e5m2": (st, [vp, u64, cbp, ctypes.POINTER(ctypes.c_double), vp, vp]),
+        "splitzip_calibrate_async": (st, [vp, u64, vp, vp, vp, vp]),
+        "splitzip_calibrate_async_e5m2": (st, [vp, u64, vp, vp, vp, vp]),
+        "splitzip_encode": (st, [vp, u64, u32, cbp, sp, vp, vp]),
+        "splitzip_encode_e5m2": (st, [vp, u64, u32, cbp, sp, vp, vp]),
+        "splitzip_encode_test": (st, [vp, u64, u32, cbp, sp, vp, vp, i32,
+                                      ctypes.POINTER(EncodeTestOpts)]),
+        "splitzip_encode_status": (st, [vp, vp, ctypes.POINTER(u64)]),
+        "splitzip_decode": (st, [sp, u64, u32, cbp, vp, vp]),
+        "splitzip_decode_e5m2": (st, [sp, u64, u32, cbp, vp, vp]),
+        "splitzip_version": (i32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise SplitZipError(status, what)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, what: str) -> ctypes.c_void_p:
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _fmt_of(x: torch.Tensor, fmt: str | None) -> str:
+    if fmt is not None:
+        return fmt
+    if x.dtype in (torch.bfloat16, torch.int16, torch.uint16):
+        return "bf16"
+    if x.dtype in (torch.float8_e5m2, torch.uint8):
+        return "e5m2"
+    raise TypeError(f"unsupported dtype {x.dtype}")
+
+
+def _codebook(cb) -> Codebook:
+    c = Codebook()
+    vals = [int(v) for v in (cb.tolist() if hasattr(cb, "tolist") else cb)]
+    if len(vals) != 16:
+        raise ValueError("a codebook has 16 entries")
+    for k, v in enumerate(vals):
+        c.exp[k] = v
+    return c
+
+
+def _streams(s: dict) -> Streams:
+    out = Streams()
+    out.codes = _dev(s["codes"], "codes")
+    out.signman = _dev(s["signman"], "signman")
+    out.chunk_off = _dev(s["chunk_off"], "chunk_off")
+    cap = s["esc_pos"].numel()
+    out.esc_capacity = min(cap, s["esc_val"].numel())
+    out.esc_pos = _dev(s["esc_pos"], "esc_pos") if cap else None
+    out.esc_val = _dev(s["esc_val"], "esc_val") if cap else None
+    return out
+
+
+# ------------------------------------------------------------ sizes (host)
+
+def splitzip_workspace_bytes(n: int, chunk: int = 1024) -> int:
+    return int(library().splitzip_workspace_bytes(n, chunk))
+
+
+def splitzip_num_chunks(n: int, chunk: int) -> int:
+    return int(library().splitzip_num_chunks(n, chunk))
+
+
+def splitzip_signman_bytes(n: int, fmt: str = "bf16") -> int:
+    lib = library()
+    return int(lib.splitzip_signman_bytes(n) if fmt == "bf16" else lib.splitzip_signman_bytes_e5m2(n))
+
+
+def splitzip_compressed_bytes(n: int, chunk: int, n_escapes: int, fmt: str = "bf16") -> int:
+    lib = library()
+    fn = lib.splitzip_compressed_bytes if fmt == "bf16" else lib.splitzip_compressed_bytes_e5m2
+    return int(fn(n, chunk, n_escapes))
+
+
+def alloc_workspace(n: int, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace for n elements (zeroed once; reusable after)."""
+    return torch.zeros(splitzip_workspace_bytes(n), dtype=torch.uint8, device=device)
+
+
+def alloc_streams(n: int, chunk: int, fmt: str = "bf16", esc_capacity: int | None = None,
+                  device="cuda") -> dict:
+    """Empty stream buffers for n elements (esc_capacity defaults to n // 32 + 1024)."""
+    cap = n // 32 + 1024 if esc_capacity is None else esc_capacity
+    return {
+        "codes": torch.empty((n + 1) // 2, dtype=torch.uint8, device=device),
+        "signman": torch.empty(splitzip_signman_bytes(n, fmt), dtype=torch.uint8, device=device),
+        "esc_pos": torch.empty(cap, dtype=torch.int16, device=device),
+        "esc_val": torch.empty(cap, dtype=torch.uint8, device=device),
+        "chunk_off": torch.empty(splitzip_num_chunks(n, chunk) + 1, dtype=torch.int32, device=device),
+    }
+
+
+# ----------------------------------------------------------- entry points
+
+def splitzip_calibrate(x: torch.Tensor, workspace: torch.Tensor, fmt: str | None = None,
+                       stream=None):
+    """Codebook (list of 16 ints) and coverage of x; synchronises the stream."""
+    fmt = _fmt_of(x, fmt)
+    cb, cov = Codebook(), ctypes.c_double()
+    fn = library().splitzip_calibrate if fmt == "bf16" else library().splitzip_calibrate_e5m2
+    _check(fn(_dev(x, "x"), x.numel(), ctypes.byref(cb), ctypes.byref(cov),
+              _dev(workspace, "workspace"), _stream(stream)), "splitzip_calibrate")
+    return list(cb.exp), cov.value
+
+
+def splitzip_calibrate_async(x: torch.Tensor, cb_out: torch.Tensor, covered_out: torch.Tensor,
+                             workspace: torch.Tensor, fmt: str | None = None, stream=None):
+    """Device-side calibration: cb_out (16 uint8) and covered_out (1 int64) on the GPU."""
+    fmt = _fmt_of(x, fmt)
+    fn = (library().splitzip_calibrate_async if fmt == "bf16"
+          else library().splitzip_calibrate_async_e5m2)
+    _check(fn(_dev(x, "x"), x.numel(), _dev(cb_out, "cb_out"), _dev(covered_out, "covered_out"),
+              _dev(workspace, "workspace"), _stream(stream)), "splitzip_calibrate_async")
+
+
+def splitzip_encode(x: torch.Tensor, chunk: int, codebook, streams: dict,
+                    workspace: torch.Tensor, fmt: str | None = None, stream=None):
+    """Enqueue one encode of x into `streams` (see alloc_streams); asynchronous."""
+    fmt = _fmt_of(x, fmt)
+    fn = library().splitzip_encode if fmt == "bf16" else library().splitzip_encode_e5m2
+    s = _streams(streams)
+    _check(fn(_dev(x, "x"), x.numel(), chunk, ctypes.byref(_codebook(codebook)),
+              ctypes.byref(s), _dev(workspace, "workspace"), _stream(stream)), "splitzip_encode")
+
+
+def splitzip_encode_test(x, chunk, codebook, streams, workspace, fmt=None, stream=None,
+                         spin_limit=0, flags=0):
+    """splitzip_encode with the test controls of include/splitzip_testing.h."""
+    fmt = _fmt_of(x, fmt)
+    s, o = _streams(streams), EncodeTestOpts(spin_limit, flags)
+    _check(library().splitzip_encode_test(
+        _dev(x, "x"), x.numel(), chunk, ctypes.byref(_codebook(codebook)), ctypes.byref(s),
+        _dev(workspace, "workspace"), _stream(stream), int(fmt == "e5m2"), ctypes.byref(o)),
+        "splitzip_encode_test")
+
+
+def splitzip_encode_status(workspace: torch.Tensor, stream=None):
+    """(status, E) of the last finished encode on this workspace; synchronises."""
+    e = ctypes.c_uint64()
+    st = library().splitzip_encode_status(_dev(workspace, "workspace"), _stream(stream),
+                                          ctypes.byref(e))
+    return int(st), int(e.value)
+
+
+def splitzip_decode(streams: dict, n: int, chunk: int, codebook, y: torch.Tensor,
+                    fmt: str = "bf16", stream=None, n_escapes: int | None = None):
+    """Enqueue one decode of `streams` into y (n elements); asynchronous.
+
+    n_escapes bounds the escape entries the kernel may read (default: the
+    capacity of the escape buffers)."""
+    s = _streams(streams)
+    if n_escapes is not None:
+        s.esc_capacity = min(s.esc_capacity, n_escapes)
+    fn = library().splitzip_decode if fmt == "bf16" else library().splitzip_decode_e5m2
+    _check(fn(ctypes.byref(s), n, chunk, ctypes.byref(_codebook(codebook)), _dev(y, "y"),
+              _stream(stream)), "splitzip_decode")
+
+
+def splitzip_version() -> int:
+    return int(library().splitzip_version())
+
+
+# ------------------------------------------------------------- codec object
+
+@dataclass
+class Encoded:
+    """One encoded tensor: device streams plus what decode needs to restore it."""
+    fmt: str
+    shape: tuple
+    dtype: torch.dtype
+    n: int
+    chunk: int
+    codebook: list
+    streams: dict
+    n_escapes: int
+
+    @property
+    def compressed_bytes(self) -> int:
+        """ceil(n/2) + sign/mantissa bytes + 3E + 4(C+1) (codebook not counted)."""
+        return splitzip_compressed_bytes(self.n, self.chunk, self.n_escapes, self.fmt)
+
+    @property
+    def ratio(self) -> float:
+        return self.n * (2 if self.fmt == "bf16" else 1) / self.compressed_bytes
+
+
+class ChunkLocalSplitZipGPU:
+    """Stateful codec with a calibrated codebook, as in the pages' Codec API:
+    ``coverage = codec.calibrate(x)``, ``enc = codec.encode(x)``,
+    ``y = codec.decode(enc)``, ``enc.compressed_bytes``."""
+
+    def __init__(self, device="cuda", chunk_size: int = 1024, fmt: str = "bf16"):
+        if fmt not in ("bf16", "e5m2"):
+            raise ValueError("fmt is 'bf16' or 'e5m2'")
+        self.device = torch.device(device)
+        self.chunk_size = int(chunk_size)
+        self.fmt = fmt
+        self.codebook = None
+        self._ws = None
+
+    def _workspace(self, n: int) -> torch.Tensor:
+        need = splitzip_workspace_bytes(n, self.chunk_size)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def _flat(self, x: torch.Tensor) -> torch.Tensor:
+        want = torch.bfloat16 if self.fmt == "bf16" else torch.float8_e5m2
+        if x.dtype != want:
+            raise TypeError(f"expected {want}, got {x.dtype}")
+        return x.reshape(-1) if x.is_contiguous() else x.contiguous().reshape(-1)
+
+    def calibrate(self, x: torch.Tensor) -> float:
+        flat = self._flat(x)
+        self.codebook, coverage = splitzip_calibrate(flat, self._workspace(flat.numel()),
+                                                     self.fmt)
+        return coverage
+
+    def encode(self, x: torch.Tensor, esc_capacity: int | None = None, stream=None) -> Encoded:
+        """Encodes x and synchronises once to read E; retries with the exact
+        escape capacity if the first guess overflowed."""
+        if self.codebook is None:
+            raise RuntimeError("calibrate() first")
+        flat = self._flat(x)
+        n = flat.numel()
+        ws = self._workspace(n)
+        streams = alloc_streams(n, self.chunk_size, self.fmt, esc_capacity, self.device)
+        splitzip_encode(flat, self.chunk_size, self.codebook, streams, ws, self.fmt, stream)
+        status, E = splitzip_encode_status(ws, stream)
+        if status == ERR_ESCAPE_OVERFLOW:
+            streams = alloc_streams(n, self.chunk_size, self.fmt, E, self.device)
+            splitzip_encode(flat, self.chunk_size, self.codebook, streams, ws, self.fmt, stream)
+            status, E = splitzip_encode_status(ws, stream)
+        _check(status, "encode")
+        streams["esc_pos"] = streams["esc_pos"][:E]
+        streams["esc_val"] = streams["esc_val"][:E]
+        return Encoded(self.fmt, tuple(x.shape), x.dtype, n, self.chunk_size,
+                       list(self.codebook), streams, E)
+
+    def decode(self, enc: Encoded, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty(enc.shape, dtype=enc.dtype, device=self.device)
+        splitzip_decode(enc.streams, enc.n, enc.chunk, enc.codebook, out.view(-1), enc.fmt,
+                        stream, enc.n_escapes)
+        return out

@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the oracle on
+the same seeded inputs.  Integer/byte work, so the bar is exact: every stream
+byte-identical, every decode bit-exact, calibration identical."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_bf16_kv_gb300 import synth
+from tests.gpu_helpers import (check_roundtrip, gpu_calibrate, gpu_encode, host_bits,
+                               assert_streams_equal)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _oracle_cb(t: torch.Tensor):
+    fmt = "bf16" if t.dtype == torch.bfloat16 else "e5m2"
+    cb, cov = oracle.calibrate(host_bits(t), fmt)
+    return cb, cov
+
+
+# ---------------------------------------------------------------- calibrate
+
+@pytest.mark.parametrize("make", [
+    lambda: synth.normal_bf16((1024, 4096), seed=1, device=DEV),
+    lambda: synth.kv_cache(1, 32768, seed=1, device=DEV),
+    lambda: synth.kv_cache(2, 1000, seed=1, device=DEV, dtype=torch.float8_e5m2),
+    lambda: synth.all_bf16_patterns().to(DEV),
+    lambda: synth.all_e5m2_patterns().to(DEV),
+    lambda: synth.normal_bf16((3,), seed=5, device=DEV),
+    lambda: synth.student_t_scaled_bf16((100001,), seed=2, device=DEV),
+], ids=["n01", "kv_layer", "kv_e5m2", "all_bf16", "all_e5m2", "n3", "t15_odd"])
+def test_calibrate_matches_oracle(make):
+    x = make()
+    cb, cov = gpu_calibrate(x)
+    ref_cb, ref_cov = _oracle_cb(x)
+    np.testing.assert_array_equal(np.array(cb, np.uint8), ref_cb)
+    assert cov == ref_cov
+
+
+# ------------------------------------------------------------ workloads
+
+@pytest.mark.parametrize("name", ["n01_1024x4096", "kv_layer_32k", "escape_stress_t15",
+                                  "escape_stress_t15_u4"])
+def test_workload_roundtrip(name):
+    w = synth.WORKLOADS[name]
+    x = w.make(DEV)
+    cb, _ = gpu_calibrate(w.make_calib(DEV))
+    ref_cb, _ = _oracle_cb(w.make_calib(DEV))
+    np.testing.assert_array_equal(np.array(cb, np.uint8), ref_cb)
+    E = check_roundtrip(x, w.chunk, cb, name)
+    assert 0 <= E <= x.numel()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
+def test_all_patterns_roundtrip(fmt):
+    x = (synth.all_bf16_patterns() if fmt == "bf16" else synth.all_e5m2_patterns()).to(DEV)
+    cb, _ = gpu_calibrate(x)
+    for chunk in (8, 64, 1024, 65536):
+        check_roundtrip(x, chunk, cb, f"{fmt} all patterns chunk {chunk}")
+    kv = synth.kv_cache(1, 64, seed=1, device=DEV,
+                        dtype=torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2)
+    cb2, _ = gpu_calibrate(kv)
+    check_roundtrip(x, 1024, cb2, f"{fmt} all patterns, KV codebook")
+
+
+SMALL_N = [1, 2, 3, 7, 8, 9, 15, 16, 17, 31, 32, 33, 1000, 8191, 8192, 8193, 16383, 16384,
+           16385, 100003]
+CHUNKS = [8, 24, 1024, 4096, 65528, 65536]
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
+@pytest.mark.parametrize("chunk", CHUNKS)
+def test_small_shapes(fmt, chunk):
+    dt = torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2
+    for n in SMALL_N:
+        # Wide exponent spread so that every size has escapes in several chunks.
+        x32 = synth.student_t_scaled_bf16((n,), seed=n, u_lo=-6, u_hi=6, device=DEV).float()
+        x = x32.to(dt)
+        cal = synth.kv_cache(1, 8, seed=1, device=DEV, dtype=dt)
+        cb, _ = gpu_calibrate(cal)
+        check_roundtrip(x, chunk, cb, f"{fmt} n={n} chunk={chunk}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
+def test_multi_tile_ragged(fmt):
+    # Several encode/decode tiles plus a ragged tail, chunk sizes that do and
+    # do not divide the tile.
+    dt = torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2
+    x = synth.kv_cache(1, 777, seed=3, device=DEV, dtype=dt).reshape(-1)[:1_500_007]
+    cb, _ = gpu_calibrate(synth.kv_cache(1, 64, seed=1, device=DEV, dtype=dt))
+    for chunk in (8, 40, 1000, 1024, 3000, 65536):
+        check_roundtrip(x, chunk, cb, f"{fmt} ragged chunk {chunk}")
+
+
+def test_zero_and_all_escape_tensors():
+    cb = list(range(100, 116))
+    zeros = torch.zeros(50000, dtype=torch.bfloat16, device=DEV)  # exponent 0: all escapes
+    assert check_roundtrip(zeros, 1024, cb, "all escapes") == 50000
+    ones = torch.ones(50000, dtype=torch.bfloat16, device=DEV)    # exponent 127: none
+    cb2 = list(range(120, 136))
+    assert check_roundtrip(ones, 1024, cb2, "no escapes") == 0
+
+
+def test_deterministic_and_workspace_reuse():
+    """Back-to-back encodes on one workspace, with different sizes and
+    formats, give identical streams every time."""
+    from lossless_bf16_kv_gb300 import splitzip as sz
+    ws = sz.alloc_workspace(3_000_000, DEV)
+    xs = [synth.kv_cache(1, 1000, seed=s, device=DEV).reshape(-1)[: 1_000_000 + 777 * s]
+          for s in range(3)]
+    xs.append(synth.kv_cache(1, 1000, seed=9, device=DEV, dtype=torch.float8_e5m2).reshape(-1))
+    cbs = [gpu_calibrate(x)[0] for x in xs]
+    first = [gpu_encode(x, 1024, cb, ws=ws)[0] for x, cb in zip(xs, cbs)]
+    for _ in range(3):
+        for x, cb, ref in zip(xs, cbs, first):
+            again, status, _, _ = gpu_encode(x, 1024, cb, ws=ws)
+            assert status == sz.OK
+            assert_streams_equal(again, ref, "repeat")
+
+
+# ------------------------------------------------ full-size configurations
+
+@pytest.mark.parametrize("name", ["kv_prefill_64L_16k", "kv_prefill_64L_16k_e5m2"])
+def test_full_size_prefill(name):
+    """2^31 elements, the launch configuration the benchmark times: every
+    stream compared in full with the oracle's."""
+    w = synth.WORKLOADS[name]
+    cal = w.make_calib(DEV)
+    cb, cov = gpu_calibrate(cal)
+    ref_cb, ref_cov = _oracle_cb(cal)
+    np.testing.assert_array_equal(np.array(cb, np.uint8), ref_cb)
+    assert cov == ref_cov
+    del cal
+    x = w.make(DEV)
+    check_roundtrip(x, w.chunk, cb, name)
