@@ -29,7 +29,7 @@ def test_invalid_arguments_are_rejected():
     x, cb = _setup()
     n = x.numel()
     ws = sz.alloc_workspace(n, DEV)
-    st = sz.alloc_streams(n, 1024)
+    st = sz.alloc_streams(n, 1024, esc_capacity=n)
     lib = sz.library()
     s = sz._streams(st)
     good_cb = sz._codebook(cb)
@@ -86,7 +86,7 @@ def test_lookback_wait_gives_up(fmt):
     x, cb = _setup(n=40_000, fmt=fmt)
     n = x.numel()
     ws = sz.alloc_workspace(n, DEV)
-    st = sz.alloc_streams(n, 1024, fmt)
+    st = sz.alloc_streams(n, 1024, fmt, esc_capacity=n)
     sz.splitzip_encode_test(x, 1024, cb, st, ws, fmt, spin_limit=2000,
                             flags=sz.TEST_STALL_FIRST_TILE)
     status, _ = sz.splitzip_encode_status(ws)
