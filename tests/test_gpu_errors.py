@@ -93,7 +93,7 @@ def test_lookback_wait_gives_up(fmt):
     assert status == sz.ERR_TIMEOUT
     # Same workspace, normal call: correct again.
     ref = oracle.encode(host_bits(x), 1024, np.asarray(cb, np.uint8), fmt)
-    gpu, status, _, _ = gpu_encode(x, 1024, cb, ws=ws)
+    gpu, status, _, _ = gpu_encode(x, 1024, cb, esc_capacity=n, ws=ws)
     assert status == sz.OK
     assert_streams_equal(gpu, ref, "after timeout")
 
