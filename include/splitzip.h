@@ -62,7 +62,8 @@ typedef enum splitzip_status {
     SPLITZIP_ERR_ESCAPE_OVERFLOW = 2, /* E > esc_capacity: escapes past capacity dropped */
     SPLITZIP_ERR_TIMEOUT = 3,         /* a bounded device wait gave up: streams invalid */
     SPLITZIP_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed */
-    SPLITZIP_ERR_WORKSPACE = 5        /* workspace not zero-initialised (or overwritten) */
+    SPLITZIP_ERR_WORKSPACE = 5,       /* workspace not zero-initialised (or overwritten) */
+    SPLITZIP_ERR_TOO_LARGE = 6        /* n above SPLITZIP_NOALLOC_MAX_ELEMENTS (no-allocation encode) */
 } splitzip_status;
 
 /* Largest chunk size: positions are uint16 within a chunk. */
@@ -177,6 +178,36 @@ splitzip_status splitzip_decode(const splitzip_streams *in, uint64_t n, uint32_t
 splitzip_status splitzip_decode_e5m2(const splitzip_streams *in, uint64_t n,
                                      uint32_t chunk_size, const splitzip_codebook *cb,
                                      void *d_y, splitzip_stream_t s);
+
+/* ------------------------------------------------ encode without workspace */
+
+/* Largest n accepted by splitzip_encode_noalloc (2^31 BF16 elements, 4 GiB). */
+#define SPLITZIP_NOALLOC_MAX_ELEMENTS (1ull << 31)
+
+/* BF16 encode for callers that cannot allocate device memory when they encode
+ * -- for example a serving engine's KV-transfer hook running while the
+ * engine's own memory pool owns the device (a cudaMalloc there may fail or
+ * stall every stream), or a plugin that is handed only its input and output
+ * buffers.  The method's pages have no counterpart of this entry point.
+ *
+ * Same streams, arguments and results as splitzip_encode, but no workspace:
+ * the scratch lives in a fixed array inside the library (about 2 MiB, held by
+ * every GPU that loads the library until the process exits), so n may not
+ * exceed SPLITZIP_NOALLOC_MAX_ELEMENTS (SPLITZIP_ERR_TOO_LARGE otherwise).
+ * Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array, which keeps the last call's
+ * contents; each call clears what must start at zero, but calls that overlap
+ * on the GPU (different streams or threads) race and must not be issued.
+ * d_status_out (4-byte aligned device memory, may be NULL) receives the
+ * device-side status bits of this encode once it finishes: 0 = success,
+ * bit 0 (1) = escape overflow (E > esc_capacity), bit 1 (2) = a bounded wait
+ * gave up (streams invalid).  E is chunk_off[C], as for splitzip_encode. */
+splitzip_status splitzip_encode_noalloc(const void *d_x, uint64_t n, uint32_t chunk_size,
+                                        const splitzip_codebook *cb,
+                                        const splitzip_streams *out, uint32_t *d_status_out,
+                                        splitzip_stream_t s);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int splitzip_version(void);

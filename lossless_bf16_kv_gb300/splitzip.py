@@ -21,9 +21,11 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIBPATH = os.path.join(_PKG, "_lib", "libsplitzip.so")
 
-OK, ERR_INVALID_ARG, ERR_ESCAPE_OVERFLOW, ERR_TIMEOUT, ERR_CUDA, ERR_WORKSPACE = range(6)
+(OK, ERR_INVALID_ARG, ERR_ESCAPE_OVERFLOW, ERR_TIMEOUT, ERR_CUDA, ERR_WORKSPACE,
+ ERR_TOO_LARGE) = range(7)
 STATUS_NAMES = {OK: "OK", ERR_INVALID_ARG: "INVALID_ARG", ERR_ESCAPE_OVERFLOW: "ESCAPE_OVERFLOW",
-                ERR_TIMEOUT: "TIMEOUT", ERR_CUDA: "CUDA", ERR_WORKSPACE: "WORKSPACE"}
+                ERR_TIMEOUT: "TIMEOUT", ERR_CUDA: "CUDA", ERR_WORKSPACE: "WORKSPACE",
+                ERR_TOO_LARGE: "TOO_LARGE"}
 MAX_CHUNK = 65536
 MAX_ELEMENTS = 0xFFFFFFFF
 TEST_STALL_FIRST_TILE = 0x1
@@ -84,6 +86,7 @@ def library() -> ctypes.CDLL:
         "splitzip_encode_status": (st, [vp, vp, ctypes.POINTER(u64)]),
         "splitzip_decode": (st, [sp, u64, u32, cbp, vp, vp]),
         "splitzip_decode_e5m2": (st, [sp, u64, u32, cbp, vp, vp]),
+        "splitzip_encode_noalloc": (st, [vp, u64, u32, cbp, sp, vp, vp]),
         "splitzip_version": (i32, []),
     }
     for name, (res, args) in sig.items():
