@@ -130,6 +130,17 @@ WORKLOADS = {
         lambda d: kv_cache(64, 1024, seed=1, device=d),
         "64-layer prefill KV BF16 [64, 2, 16384, 8, 128] (2^31 elements, 4.29 GB); "
         "codebook from a [64, 2, 1024, 8, 128] seed-1 sample"),
+    "kv_prefill_4L_16k": Workload(
+        "kv_prefill_4L_16k", "bf16", (4, 2, 16384, 8, 128), 1024,
+        lambda d: kv_cache(4, 16384, seed=0, device=d),
+        lambda d: kv_cache(4, 1024, seed=1, device=d),
+        "4-layer prefill KV BF16 [4, 2, 16384, 8, 128] (2^27 elements, 268 MB > L2): the "
+        "profiling-size cut of the 64-layer workload"),
+    "kv_prefill_4L_16k_e5m2": Workload(
+        "kv_prefill_4L_16k_e5m2", "e5m2", (4, 2, 16384, 8, 128), 1024,
+        lambda d: kv_cache(4, 16384, seed=0, device=d, dtype=torch.float8_e5m2),
+        lambda d: kv_cache(4, 1024, seed=1, device=d, dtype=torch.float8_e5m2),
+        "4-layer prefill KV E5M2 (2^27 elements, 134 MB > L2): profiling-size cut"),
     "escape_stress_t15": Workload(
         "escape_stress_t15", "bf16", (8192, 8192), 1024,
         lambda d: student_t_scaled_bf16((8192, 8192), seed=0, device=d), _n01_calib,
