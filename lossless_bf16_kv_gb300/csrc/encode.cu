@@ -6,22 +6,28 @@
 // exponent through the 16-entry codebook to a 4-bit code, and send exponents
 // outside the codebook to a chunk-local escape stream of (position, value).
 //
-// One launch, one pass over the input.  Each CTA takes a tile (8192 BF16 or
-// 16384 E5M2 elements) by atomic ticket, so every tile a CTA can wait on
-// belongs to a CTA that has already started.  Per tile:
-//   1. 16-byte loads of the input; SWAR field split; exponent -> code lookup
-//      in a 256-entry shared-memory table (entry 0x10 marks an escape);
-//      nibble packing; the dense code and sign+mantissa streams are stored
-//      right away (fixed offsets, no dependence on other tiles).
-//   2. Escape counts per thread group; a block-wide scan gives each group's
-//      rank inside the tile; warp 0 publishes the tile's count and runs a
-//      decoupled look-back (Merrill & Garland, "Single-pass Parallel Prefix
-//      Scan with Decoupled Look-back", 2016) over earlier tiles' state words
-//      to get the tile's exclusive escape prefix.
-//   3. Escapes are written compacted at their global ranks, and chunk_off is
-//      written at every chunk boundary inside the tile.
-// Escapes are therefore in element order, which is chunk order then position
-// order within a chunk, for any chunk size.
+// One launch, one pass over the input, persistent CTAs (two per SM), each a
+// warp-specialised pipeline over 8192-element tiles claimed by atomic ticket:
+//   producer warp   claims tiles and streams each tile's input into a
+//                   three-stage shared-memory ring with bulk copies
+//                   (cp.async.bulk + mbarrier);
+//   8 compute warps split the fields (byte permutes), look the exponents up in
+//                   a 256-entry shared table, pack the nibbles and store the
+//                   dense code and sign+mantissa streams (fixed offsets); they
+//                   count escapes, rank them with a block scan and drop them,
+//                   with the rank of every chunk boundary, into one of two
+//                   shared-memory escape slots, then go straight on to the
+//                   next tile;
+//   look-back warp  takes a filled slot, publishes the tile's escape count and
+//                   runs a decoupled look-back (Merrill & Garland, "Single-pass
+//                   Parallel Prefix Scan with Decoupled Look-back", 2016) over
+//                   earlier tiles' state words for the tile's global escape
+//                   offset, then writes the slot's escapes and chunk offsets.
+// Only the look-back warp ever waits on other CTAs, and it runs one tile
+// behind the compute warps.  Escapes come out in element order, which is
+// chunk order then position order within a chunk, for any chunk size.  Every
+// wait is bounded: a wait that runs out records SPLITZIP_ERR_TIMEOUT, lets the
+// pipeline drain with every access in bounds, and returns.
 #include <cstdint>
 
 #include "common.cuh"
@@ -31,46 +37,6 @@ namespace splitzip {
 namespace {
 
 constexpr uint32_t kMissEntry = 0x10u;  // table entry of an exponent outside the codebook
-
-// ------------------------------------------------------------------ setup
-
-struct TileInfo {
-    uint32_t tile;   // tile id (ticket)
-    uint32_t epoch;  // launch epoch
-    uint32_t t0;     // first element of the tile
-    uint32_t q0;     // t0 / chunk
-    uint32_t r0;     // t0 % chunk
-};
-
-// Takes the ticket, reads the epoch and builds the exponent -> entry table.
-template <int kTile>
-__device__ __forceinline__ TileInfo tile_setup(const EncodeArgs& a, uint8_t* table,
-                                               uint32_t* s_info) {
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        const uint32_t tile = atomicAdd(&hdr->ticket, 1u);
-        const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&hdr->epoch);
-        const uint32_t t0 = tile * (uint32_t)kTile;  // tile < num_tiles keeps t0 < n < 2^32
-        const uint32_t q0 = t0 / a.cdiv.d;
-        s_info[0] = tile;
-        s_info[1] = epoch;
-        s_info[2] = t0;
-        s_info[3] = q0;
-        s_info[4] = t0 - q0 * a.cdiv.d;
-    }
-    table[tid] = (uint8_t)kMissEntry;
-    __syncthreads();
-    if (tid < 16) table[(a.cbw[tid >> 2] >> (8 * (tid & 3))) & 0xFFu] = (uint8_t)tid;
-    __syncthreads();
-    TileInfo t;
-    t.tile = s_info[0];
-    t.epoch = s_info[1];
-    t.t0 = s_info[2];
-    t.q0 = s_info[3];
-    t.r0 = s_info[4];
-    return t;
-}
 
 // Four table entries for the four exponent bytes of `ex`, one per byte.
 __device__ __forceinline__ uint32_t lookup4(const uint8_t* table, uint32_t ex) {
@@ -93,14 +59,159 @@ __device__ __forceinline__ uint32_t miss_count(uint32_t w_lo, uint32_t w_hi) {
     return __popc((w_lo & 0x10101010u) | ((w_hi & 0x10101010u) >> 1));
 }
 
-// ------------------------------------------------------- block-wide scan
+// ------------------------------------------------------------------- BF16
 //
-// Each thread holds counts c[k] (k < G <= 4) for its groups; group (k, t) comes
-// before (k', t') in element order iff k < k' or (k == k' and t < t').  Returns
-// the exclusive rank of each group inside the tile and the tile total.
+// Field split of 8 BF16 values (4 words, 2 values each): the low bytes of
+// elements 0..3 gather into one word and the high bytes into another, so the
+// sign+mantissa byte (sign from the high byte's bit 7, mantissa from the low
+// byte's bits 0..6) and the exponent byte (high byte bits 0..6 above low byte
+// bit 7) come out four at a time.
+__device__ __forceinline__ void split_bf16(uint32_t a, uint32_t b, uint32_t& sm, uint32_t& ex) {
+    const uint32_t lo = __byte_perm(a, b, 0x6420);
+    const uint32_t hi = __byte_perm(a, b, 0x7531);
+    sm = (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
+    ex = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
+}
+
+// 4 E5M2 bytes -> 4 exponent bytes and 4 three-bit fields packed in 12 bits
+// (field of byte k at bits 3k..3k+2).
+__device__ __forceinline__ void split_e5m2(uint32_t w, uint32_t& ex, uint32_t& f12) {
+    ex = (w >> 2) & 0x1F1F1F1Fu;
+    const uint32_t f = ((w >> 5) & 0x04040404u) | (w & 0x03030303u);  // sign<<2 | mantissa
+    const uint32_t t = f | (f >> 5);
+    f12 = (t & 0x3Fu) | ((t >> 10) & 0xFC0u);
+}
+
+// ------------------------------------------------------ decoupled look-back
+//
+// Run by all 32 lanes of the look-back warp.  Publishes the tile's aggregate,
+// then walks back over earlier tiles' state words until it meets an inclusive
+// prefix, publishes this tile's inclusive prefix and returns the exclusive
+// one.  Each poll reads a window of 32 x kLookK predecessors (lane l reads the
+// kLookK words l*kLookK ... nearest first), because with every CTA working at
+// once a tile's nearest few hundred predecessors are often all in flight and
+// carry only aggregates.  Every wait is bounded by a.spin_limit polls.
+constexpr int kLookK = 8;
+
+__device__ __forceinline__ uint32_t look_back(const EncodeArgs& a, uint32_t tile, uint32_t epoch,
+                                              uint32_t aggregate) {
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+    uint64_t* states = reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes);
+    const int lane = threadIdx.x & 31;
+    if (tile == 0) {
+        if (lane == 0 && !(a.test_flags & kTestStallFirstTile))
+            st_relaxed_gpu(states, make_state(kFlagPrefix, aggregate, epoch));
+        return 0;
+    }
+    if (lane == 0) st_relaxed_gpu(states + tile, make_state(kFlagAggregate, aggregate, epoch));
+    uint32_t excl = 0, polls = 0;
+    bool timed_out = false;
+    int64_t pred = (int64_t)tile - 1;
+    while (true) {
+        uint64_t w[kLookK];
+#pragma unroll
+        for (int m = 0; m < kLookK; m++) {
+            const int64_t idx = pred - (lane * kLookK + m);
+            w[m] = idx >= 0 ? ld_relaxed_gpu(states + idx) : make_state(kFlagPrefix, 0u, epoch);
+        }
+        // This lane's words, nearest first: sum up to and including the first
+        // inclusive prefix; stop at a word that is not ready yet.
+        uint32_t sum = 0;
+        bool has_prefix = false, not_ready = false;
+#pragma unroll
+        for (int m = 0; m < kLookK; m++) {
+            if (has_prefix || not_ready) continue;
+            const uint32_t f = state_flag(w[m], epoch);
+            if (f == 0u) {
+                not_ready = true;
+            } else {
+                sum += (uint32_t)w[m];
+                has_prefix = f == kFlagPrefix;
+            }
+        }
+        const uint32_t pm = __ballot_sync(0xFFFFFFFFu, has_prefix);
+        const uint32_t bad = __ballot_sync(0xFFFFFFFFu, not_ready);
+        // Lanes up to and including the nearest lane with a prefix (all 32 if none).
+        const uint32_t need = pm ? (((pm & (0u - pm)) << 1) - 1u) : 0xFFFFFFFFu;
+        if (bad & need) {
+            if (++polls > a.spin_limit) {
+                timed_out = true;
+                break;
+            }
+            __nanosleep(32);
+            continue;
+        }
+        excl += __reduce_add_sync(0xFFFFFFFFu, ((need >> lane) & 1u) ? sum : 0u);
+        if (pm) break;
+        pred -= 32 * kLookK;
+    }
+    if (lane == 0) {
+        if (timed_out) atomicOr(&hdr->status, kStatusTimeout);
+        // Published even after a time-out so that later tiles are not held up.
+        st_relaxed_gpu(states + tile, make_state(kFlagPrefix, excl + aggregate, epoch));
+    }
+    return excl;
+}
+
+// ------------------------------------------------------------ pipeline
+
+constexpr uint32_t kInvalidTile = 0xFFFFFFFFu;
+constexpr int kTile = 8192;                            // elements per tile, both formats
+constexpr int kStages = 3;                             // input ring depth
+constexpr int kComputeThreads = kThreads;              // 8 compute warps
+constexpr int kEncodeThreads = kComputeThreads + 64;   // + producer warp + look-back warp
+constexpr int kMaxBoundaries = kTile / 8 + 1;          // chunk starts one tile can hold
+constexpr uint64_t kWaitNs = 2000000000ull;            // an mbarrier wait gives up after 2 s
+
+template <int kElemBytes>
+struct EncodeSmem {
+    alignas(128) uint8_t stage[kStages][kTile * kElemBytes];  // input ring (bulk-copy target)
+    uint16_t list_pos[2][kTile];    // escape slots: position in chunk, by rank in tile
+    uint8_t list_val[2][kTile];     //               raw exponent
+    uint32_t bnd[2][kMaxBoundaries];  // rank in tile at each chunk start, by chunk
+    uint8_t table[256];             // exponent -> code (kMissEntry: escape)
+    uint32_t warp_tot[2][kWarps][2];
+    uint32_t stage_tile[kStages], stage_q0[kStages], stage_r0[kStages];
+    uint32_t slot_tile[2], slot_agg[2], slot_q0[2], slot_r0[2];
+    uint32_t cur_tile;
+    uint32_t err;
+    alignas(8) uint64_t full[kStages];   // producer -> compute: stage filled (tx bytes)
+    uint64_t empty[kStages];             // compute -> producer: stage consumed
+    uint64_t slot_full[2];               // compute -> look-back: slot filled (8 warps)
+    uint64_t slot_empty[2];              // look-back -> compute: slot written out
+};
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase (time-based, so the bound does not depend
+// on how long a single try_wait suspends).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        for (int i = 0; i < 64; i++)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+}
+
+template <int kElemBytes>
+__device__ __forceinline__ void record_timeout(const EncodeArgs& a, EncodeSmem<kElemBytes>& sm) {
+    atomicOr(&reinterpret_cast<WsHeader*>(a.ws)->status, kStatusTimeout);
+    *reinterpret_cast<volatile uint32_t*>(&sm.err) = 1u;
+}
+
+// Block scan over the 256 compute threads (named barrier 1).  Each thread
+// holds counts c[k] (k < G <= 4) for its groups; group (k, t) precedes
+// (k', t') in element order iff k < k' or (k == k' and t < t').  Returns the
+// tile total and each group's exclusive rank in the tile.
 template <int G>
 __device__ __forceinline__ uint32_t block_ranks(const uint32_t (&c)[G], uint32_t (&rank)[G],
-                                                uint32_t (*s_warp)[2]) {
+                                                uint32_t (*wt)[2]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t p01 = c[0] | (G > 1 ? c[1] << 16 : 0u);
     uint32_t p23 = (G > 2 ? c[2] : 0u) | (G > 3 ? c[3] << 16 : 0u);
@@ -115,14 +226,14 @@ __device__ __forceinline__ uint32_t block_ranks(const uint32_t (&c)[G], uint32_t
         }
     }
     if (lane == 31) {
-        s_warp[warp][0] = p01;
-        s_warp[warp][1] = p23;
+        wt[warp][0] = p01;
+        wt[warp][1] = p23;
     }
-    __syncthreads();
+    named_sync(1, kComputeThreads);
     uint32_t pre01 = 0, pre23 = 0, tot01 = 0, tot23 = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; w++) {
-        const uint32_t x = s_warp[w][0], y = s_warp[w][1];
+        const uint32_t x = wt[w][0], y = wt[w][1];
         if (w < warp) {
             pre01 += x;
             pre23 += y;
@@ -142,283 +253,157 @@ __device__ __forceinline__ uint32_t block_ranks(const uint32_t (&c)[G], uint32_t
     return base;
 }
 
-// ------------------------------------------------------ decoupled look-back
+// ------------------------------------------------------ per-format tiles
 //
-// Run by all 32 lanes of warp 0.  Publishes the tile's aggregate, walks back
-// over earlier tiles' state words 32 at a time until it meets an inclusive
-// prefix, publishes this tile's inclusive prefix and returns the exclusive one.
-// Every wait is bounded by a.spin_limit polls.
-__device__ __forceinline__ uint32_t look_back(const EncodeArgs& a, const TileInfo& t,
-                                              uint32_t aggregate) {
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
-    uint64_t* states = reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes);
-    const int lane = threadIdx.x & 31;
-    if (t.tile == 0) {
-        if (lane == 0 && !(a.test_flags & kTestStallFirstTile))
-            st_relaxed_gpu(states, make_state(kFlagPrefix, aggregate, t.epoch));
-        return 0;
+// BF16: thread t's groups of 8 sit at tile offsets k*2048 + 8t (k < 4), so a
+// warp reads 512 contiguous bytes of the stage per group (no bank conflicts)
+// and writes 128 contiguous code bytes and 256 sign+mantissa bytes.
+struct Bf16Tile {
+    static constexpr int kElemBytes = 2;
+    static constexpr int kGroups = 4;
+    struct Keep {
+        uint32_t ex[kGroups][2], ent[kGroups][2], cnt[kGroups];
+    };
+    static __device__ __forceinline__ uint32_t loff(int k) {
+        return k * (kThreads * 8) + threadIdx.x * 8;
     }
-    if (lane == 0) st_relaxed_gpu(states + t.tile, make_state(kFlagAggregate, aggregate, t.epoch));
-    uint32_t excl = 0, polls = 0;
-    bool timed_out = false;
-    int64_t pred = (int64_t)t.tile - 1;
-    while (true) {
-        const int64_t idx = pred - lane;
-        const uint64_t w = idx >= 0 ? ld_relaxed_gpu(states + idx)
-                                    : make_state(kFlagPrefix, 0u, t.epoch);
-        const uint32_t f = state_flag(w, t.epoch);
-        const uint32_t pm = __ballot_sync(0xFFFFFFFFu, f == kFlagPrefix);
-        const uint32_t bad = __ballot_sync(0xFFFFFFFFu, f == 0u);
-        // Lanes up to and including the nearest inclusive prefix (all 32 if none).
-        const uint32_t need = pm ? (((pm & (0u - pm)) << 1) - 1u) : 0xFFFFFFFFu;
-        if (bad & need) {
-            if (++polls > a.spin_limit) {
-                timed_out = true;
-                break;
+
+    static __device__ __forceinline__ void process(const EncodeArgs& a, const uint8_t* stage,
+                                                   const uint8_t* table, uint32_t t0, Keep& kp) {
+        const bool full = (uint64_t)t0 + kTile <= a.n;
+        const uint32_t pad = (a.cbw[0] & 0xFFu) << 7;  // exponent cb[0], sign 0, mantissa 0: code 0
+#pragma unroll
+        for (int k = 0; k < kGroups; k++) {
+            const uint32_t l = loff(k), i = t0 + l;
+            kp.cnt[k] = 0;
+            kp.ent[k][0] = kp.ent[k][1] = 0;
+            if (!full && i >= a.n) continue;
+            uint4 v;
+            const bool whole = full || i + 8 <= a.n;
+            if (whole) {
+                v = *reinterpret_cast<const uint4*>(stage + 2 * l);
+            } else {
+                const uint16_t* h = reinterpret_cast<const uint16_t*>(stage) + l;
+                const uint32_t rem = a.n - i;
+                uint32_t w[4];
+#pragma unroll
+                for (int m = 0; m < 4; m++)
+                    w[m] = (2 * m < (int)rem ? h[2 * m] : pad) |
+                           ((2 * m + 1 < (int)rem ? (uint32_t)h[2 * m + 1] : pad) << 16);
+                v = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            __nanosleep(100);
-            continue;
-        }
-        excl += __reduce_add_sync(0xFFFFFFFFu, ((need >> lane) & 1u) ? (uint32_t)w : 0u);
-        if (pm) break;
-        pred -= 32;
-    }
-    if (lane == 0) {
-        if (timed_out) atomicOr(&hdr->status, kStatusTimeout);
-        // Published even after a time-out so that later tiles are not held up.
-        st_relaxed_gpu(states + t.tile, make_state(kFlagPrefix, excl + aggregate, t.epoch));
-    }
-    return excl;
-}
-
-// CTA exit bookkeeping (thread 0): the last CTA to finish moves the status
-// bits out and re-arms the header for the next launch.
-__device__ __forceinline__ void count_finished(const EncodeArgs& a, uint32_t epoch) {
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
-    __threadfence();
-    const uint32_t prev = atomicAdd(&hdr->done, 1u);
-    if (prev == a.num_tiles - 1) {
-        __threadfence();
-        hdr->last_status = atomicExch(&hdr->status, 0u);
-        hdr->ticket = 0;
-        hdr->done = 0;
-        hdr->epoch = epoch + 1u;
-        __threadfence();
-    }
-}
-
-// End of a tile: the tile holding the last element records E and the
-// overflow bit, then the CTA counts itself finished.
-__device__ __forceinline__ void tile_finish(const EncodeArgs& a, const TileInfo& t,
-                                            uint32_t total) {
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
-    if (threadIdx.x != 0) return;
-    if (t.tile == a.num_tiles - 1) {
-        a.chunk_off[a.nchunks] = total;
-        hdr->last_escapes = total;
-        if ((uint64_t)total > a.esc_capacity) atomicOr(&hdr->status, kStatusOverflow);
-    }
-    count_finished(a, t.epoch);
-}
-
-// A ticket at or past the grid size means the header did not start zeroed:
-// touch nothing but the header, and report it.
-__device__ __forceinline__ bool stray_tile(const EncodeArgs& a, const TileInfo& t) {
-    if (t.tile < a.num_tiles) return false;
-    if (threadIdx.x == 0) {
-        atomicOr(&reinterpret_cast<WsHeader*>(a.ws)->status, kStatusBadWorkspace);
-        count_finished(a, t.epoch);
-    }
-    return true;
-}
-
-__device__ __forceinline__ void put_escape(const EncodeArgs& a, uint32_t rank, uint32_t pos,
-                                           uint32_t e) {
-    if ((uint64_t)rank < a.esc_capacity) {
-        a.esc_pos[rank] = (uint16_t)pos;
-        a.esc_val[rank] = (uint8_t)e;
-    }
-}
-
-// ------------------------------------------------------------------- BF16
-//
-// Field split of 8 BF16 values (4 words, 2 values each): the low bytes of
-// elements 0..3 gather into one word and the high bytes into another, so the
-// sign+mantissa byte (sign from the high byte's bit 7, mantissa from the low
-// byte's bits 0..6) and the exponent byte (high byte bits 0..6 above low byte
-// bit 7) come out four at a time.
-__device__ __forceinline__ void split_bf16(uint32_t a, uint32_t b, uint32_t& sm, uint32_t& ex) {
-    const uint32_t lo = __byte_perm(a, b, 0x6420);
-    const uint32_t hi = __byte_perm(a, b, 0x7531);
-    sm = (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
-    ex = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
-}
-
-constexpr int kBf16Groups = 4;                              // groups of 8 per thread
-constexpr int kBf16Tile = kThreads * kBf16Groups * 8;      // 8192 elements
-constexpr uint32_t kBf16Stride = kThreads * 8;             // elements between a thread's groups
-
-__global__ void __launch_bounds__(kThreads) encode_bf16_kernel(const EncodeArgs a) {
-    __shared__ uint8_t table[256];
-    __shared__ uint32_t s_info[5];
-    __shared__ uint32_t s_warp[kWarps][2];
-    __shared__ uint32_t s_excl;
-
-    const TileInfo t = tile_setup<kBf16Tile>(a, table, s_info);
-    if (stray_tile(a, t)) return;
-    const int tid = threadIdx.x;
-    const uint32_t pad = (a.cbw[0] & 0xFFu) << 7;  // exponent cb[0], sign 0, mantissa 0: code 0
-    const bool full = (uint64_t)t.t0 + kBf16Tile <= a.n;
-
-    uint32_t ex[kBf16Groups][2], ent[kBf16Groups][2], cnt[kBf16Groups];
-#pragma unroll
-    for (int k = 0; k < kBf16Groups; k++) {
-        const uint32_t i = t.t0 + k * kBf16Stride + tid * 8;
-        uint4 v;
-        if (full || i + 8 <= a.n) {
-            v = ld_stream16(a.x + 2ull * i);
-        } else {
-            uint16_t h[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                h[j] = (i < a.n && j < (int)(a.n - i))
-                           ? reinterpret_cast<const uint16_t*>(a.x)[i + j]
-                           : (uint16_t)pad;
-            v.x = h[0] | ((uint32_t)h[1] << 16);
-            v.y = h[2] | ((uint32_t)h[3] << 16);
-            v.z = h[4] | ((uint32_t)h[5] << 16);
-            v.w = h[6] | ((uint32_t)h[7] << 16);
-        }
-        uint32_t sm0, sm1;
-        split_bf16(v.x, v.y, sm0, ex[k][0]);
-        split_bf16(v.z, v.w, sm1, ex[k][1]);
-        ent[k][0] = lookup4(table, ex[k][0]);
-        ent[k][1] = lookup4(table, ex[k][1]);
-        const uint32_t codes = pack_nibbles(ent[k][0], ent[k][1]);
-        cnt[k] = miss_count(ent[k][0], ent[k][1]);
-        if (full || i + 8 <= a.n) {
-            st_stream4(a.codes + i / 2, codes);
-            st_stream8(a.signman + i, make_uint2(sm0, sm1));
-        } else if (i < a.n) {
-            const uint32_t rem = a.n - i;
-            for (uint32_t j = 0; j < (rem + 1) / 2; j++) a.codes[i / 2 + j] = (uint8_t)(codes >> (8 * j));
-            for (uint32_t j = 0; j < rem; j++)
-                a.signman[i + j] = (uint8_t)((j < 4 ? sm0 : sm1) >> (8 * (j & 3)));
+            uint32_t sm0, sm1;
+            split_bf16(v.x, v.y, sm0, kp.ex[k][0]);
+            split_bf16(v.z, v.w, sm1, kp.ex[k][1]);
+            kp.ent[k][0] = lookup4(table, kp.ex[k][0]);
+            kp.ent[k][1] = lookup4(table, kp.ex[k][1]);
+            const uint32_t codes = pack_nibbles(kp.ent[k][0], kp.ent[k][1]);
+            kp.cnt[k] = miss_count(kp.ent[k][0], kp.ent[k][1]);
+            if (whole) {
+                st_stream4(a.codes + i / 2, codes);
+                st_stream8(a.signman + i, make_uint2(sm0, sm1));
+            } else {
+                const uint32_t rem = a.n - i;
+                for (uint32_t j = 0; j < (rem + 1) / 2; j++) a.codes[i / 2 + j] = (uint8_t)(codes >> (8 * j));
+                for (uint32_t j = 0; j < rem; j++)
+                    a.signman[i + j] = (uint8_t)((j < 4 ? sm0 : sm1) >> (8 * (j & 3)));
+            }
         }
     }
 
-    uint32_t rank[kBf16Groups];
-    const uint32_t aggregate = block_ranks<kBf16Groups>(cnt, rank, s_warp);
-    if (tid < 32) {
-        const uint32_t excl = look_back(a, t, aggregate);
-        if (tid == 0) s_excl = excl;
-    }
-    __syncthreads();
-    const uint32_t excl = s_excl;
-
+    // Escapes into the slot at their ranks; ranks at chunk starts into bnd.
+    static __device__ __forceinline__ void emit(const EncodeArgs& a, const Keep& kp,
+                                                const uint32_t (&rank)[kGroups], uint32_t t0,
+                                                uint32_t r0, uint16_t* lpos, uint8_t* lval,
+                                                uint32_t* bnd) {
+        const bool full = (uint64_t)t0 + kTile <= a.n;
 #pragma unroll
-    for (int k = 0; k < kBf16Groups; k++) {
-        const uint32_t loff = k * kBf16Stride + tid * 8;
-        const uint32_t i = t.t0 + loff;
-        if (!full && i >= a.n) continue;
-        // A group of 8 lies inside one chunk (chunk % 8 == 0, group 8-aligned).
-        const uint32_t x = t.r0 + loff;
-        const uint32_t q = chunk_quot(a.cdiv, x);
-        const uint32_t r = x - q * a.cdiv.d;
-        uint32_t g = excl + rank[k];
-        if (r == 0) a.chunk_off[t.q0 + q] = g;
-        if (cnt[k]) {
+        for (int k = 0; k < kGroups; k++) {
+            const uint32_t l = loff(k);
+            if (!full && t0 + l >= a.n) continue;
+            // A group of 8 lies inside one chunk (chunk % 8 == 0, group 8-aligned).
+            const uint32_t x = r0 + l;
+            const uint32_t q = chunk_quot(a.cdiv, x);
+            const uint32_t r = x - q * a.cdiv.d;
+            uint32_t g = rank[k];
+            if (r == 0) bnd[q] = g;
+            if (kp.cnt[k]) {
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const uint32_t e = ent[k][j >> 2] >> (8 * (j & 3));
-                if (e & kMissEntry) {
-                    put_escape(a, g, r + j, (ex[k][j >> 2] >> (8 * (j & 3))) & 0xFFu);
-                    g++;
+                for (int j = 0; j < 8; j++) {
+                    if ((kp.ent[k][j >> 2] >> (8 * (j & 3))) & kMissEntry) {
+                        lpos[g] = (uint16_t)(r + j);
+                        lval[g] = (uint8_t)(kp.ex[k][j >> 2] >> (8 * (j & 3)));
+                        g++;
+                    }
                 }
             }
         }
     }
-    tile_finish(a, t, excl + aggregate);
-}
+};
 
-// ------------------------------------------------------------------- E5M2
-//
-// A thread group is 32 consecutive elements (two 16-byte loads): 16 code
-// bytes and 12 sign+mantissa bytes (32 three-bit fields) per group.
+// E5M2: thread t's group is the 32 elements at tile offset 32t (two 16-byte
+// stage reads): 16 code bytes and 12 bytes of packed 3-bit fields.
+struct E5m2Tile {
+    static constexpr int kElemBytes = 1;
+    static constexpr int kGroups = 1;
+    struct Keep {
+        uint32_t ex[8], ent[8], cnt[kGroups];
+    };
+    static __device__ __forceinline__ uint32_t loff() { return threadIdx.x * 32; }
 
-// 4 E5M2 bytes -> 4 exponent bytes and 4 three-bit fields packed in 12 bits
-// (field of byte k at bits 3k..3k+2).
-__device__ __forceinline__ void split_e5m2(uint32_t w, uint32_t& ex, uint32_t& f12) {
-    ex = (w >> 2) & 0x1F1F1F1Fu;
-    const uint32_t f = ((w >> 5) & 0x04040404u) | (w & 0x03030303u);  // sign<<2 | mantissa
-    const uint32_t t = f | (f >> 5);
-    f12 = (t & 0x3Fu) | ((t >> 10) & 0xFC0u);
-}
-
-constexpr int kE5m2Groups = 2;                              // groups of 32 per thread
-constexpr int kE5m2Tile = kThreads * kE5m2Groups * 32;     // 16384 elements
-constexpr uint32_t kE5m2Stride = kThreads * 32;
-
-__global__ void __launch_bounds__(kThreads) encode_e5m2_kernel(const EncodeArgs a) {
-    __shared__ uint8_t table[256];
-    __shared__ uint32_t s_info[5];
-    __shared__ uint32_t s_warp[kWarps][2];
-    __shared__ uint32_t s_excl;
-
-    const TileInfo t = tile_setup<kE5m2Tile>(a, table, s_info);
-    if (stray_tile(a, t)) return;
-    const int tid = threadIdx.x;
-    const uint32_t pad = (a.cbw[0] & 0x1Fu) << 2;  // exponent cb[0], sign 0, mantissa 0
-    const bool full = (uint64_t)t.t0 + kE5m2Tile <= a.n;
-
-    uint32_t ex[kE5m2Groups][8], ent[kE5m2Groups][8], cnt[kE5m2Groups];
+    static __device__ __forceinline__ void process(const EncodeArgs& a, const uint8_t* stage,
+                                                   const uint8_t* table, uint32_t t0, Keep& kp) {
+        const bool full = (uint64_t)t0 + kTile <= a.n;
+        const uint32_t l = loff(), i = t0 + l;
+        kp.cnt[0] = 0;
 #pragma unroll
-    for (int k = 0; k < kE5m2Groups; k++) {
-        const uint32_t i = t.t0 + k * kE5m2Stride + tid * 32;
+        for (int m = 0; m < 8; m++) kp.ent[m] = 0;
+        if (!full && i >= a.n) return;
+        const bool whole = full || i + 32 <= a.n;
         uint32_t w[8];
-        if (full || i + 32 <= a.n) {
-            const uint4 v0 = ld_stream16(a.x + i);
-            const uint4 v1 = ld_stream16(a.x + i + 16);
+        if (whole) {
+            const uint4 v0 = *reinterpret_cast<const uint4*>(stage + l);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(stage + l + 16);
             w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
             w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
         } else {
+            const uint32_t pad = (a.cbw[0] & 0x1Fu) << 2;  // exponent cb[0], sign 0, mantissa 0
+            const uint32_t rem = a.n - i;
 #pragma unroll
             for (int m = 0; m < 8; m++) {
                 uint32_t acc = 0;
 #pragma unroll
                 for (int b = 0; b < 4; b++) {
                     const uint32_t j = m * 4 + b;
-                    const uint32_t byte = (i < a.n && j < a.n - i) ? a.x[i + j] : pad;
-                    acc |= byte << (8 * b);
+                    acc |= (j < rem ? (uint32_t)stage[l + j] : pad) << (8 * b);
                 }
                 w[m] = acc;
             }
         }
         uint32_t f12[8];
-        cnt[k] = 0;
 #pragma unroll
         for (int m = 0; m < 8; m++) {
-            split_e5m2(w[m], ex[k][m], f12[m]);
-            ent[k][m] = lookup4(table, ex[k][m]);
+            split_e5m2(w[m], kp.ex[m], f12[m]);
+            kp.ent[m] = lookup4(table, kp.ex[m]);
         }
         uint4 codes;
-        codes.x = pack_nibbles(ent[k][0], ent[k][1]);
-        codes.y = pack_nibbles(ent[k][2], ent[k][3]);
-        codes.z = pack_nibbles(ent[k][4], ent[k][5]);
-        codes.w = pack_nibbles(ent[k][6], ent[k][7]);
+        codes.x = pack_nibbles(kp.ent[0], kp.ent[1]);
+        codes.y = pack_nibbles(kp.ent[2], kp.ent[3]);
+        codes.z = pack_nibbles(kp.ent[4], kp.ent[5]);
+        codes.w = pack_nibbles(kp.ent[6], kp.ent[7]);
 #pragma unroll
-        for (int m = 0; m < 8; m += 2) cnt[k] += miss_count(ent[k][m], ent[k][m + 1]);
+        for (int m = 0; m < 8; m += 2) kp.cnt[0] += miss_count(kp.ent[m], kp.ent[m + 1]);
         // 8 x 12 bits -> 96 bits, little-endian.
         const uint32_t s0 = f12[0] | (f12[1] << 12) | (f12[2] << 24);
         const uint32_t s1 = (f12[2] >> 8) | (f12[3] << 4) | (f12[4] << 16) | (f12[5] << 28);
         const uint32_t s2 = (f12[5] >> 4) | (f12[6] << 8) | (f12[7] << 20);
         uint8_t* smp = a.signman + (uint64_t)(i / 32) * 12;
-        if (full || i + 32 <= a.n) {
+        if (whole) {
             st_stream16(a.codes + i / 2, codes);
             st_stream4(smp, s0);
             st_stream4(smp + 4, s1);
             st_stream4(smp + 8, s2);
-        } else if (i < a.n) {
+        } else {
             const uint32_t rem = a.n - i;
             const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
             for (uint32_t j = 0; j < (rem + 1) / 2; j++)
@@ -429,56 +414,253 @@ __global__ void __launch_bounds__(kThreads) encode_e5m2_kernel(const EncodeArgs 
         }
     }
 
-    uint32_t rank[kE5m2Groups];
-    const uint32_t aggregate = block_ranks<kE5m2Groups>(cnt, rank, s_warp);
-    if (tid < 32) {
-        const uint32_t excl = look_back(a, t, aggregate);
-        if (tid == 0) s_excl = excl;
-    }
-    __syncthreads();
-    const uint32_t excl = s_excl;
-
-#pragma unroll
-    for (int k = 0; k < kE5m2Groups; k++) {
-        const uint32_t loff = k * kE5m2Stride + tid * 32;
-        const uint32_t i = t.t0 + loff;
-        if (!full && i >= a.n) continue;
-        uint32_t g = excl + rank[k];
+    static __device__ __forceinline__ void emit(const EncodeArgs& a, const Keep& kp,
+                                                const uint32_t (&rank)[kGroups], uint32_t t0,
+                                                uint32_t r0, uint16_t* lpos, uint8_t* lval,
+                                                uint32_t* bnd) {
+        const bool full = (uint64_t)t0 + kTile <= a.n;
+        const uint32_t l = loff();
+        if (!full && t0 + l >= a.n) return;
+        uint32_t g = rank[0];
         // Four runs of 8 elements; each lies inside one chunk.
 #pragma unroll
         for (int s = 0; s < 4; s++) {
-            if (!full && i + 8 * s >= a.n) break;
-            const uint32_t x = t.r0 + loff + 8 * s;
+            if (!full && t0 + l + 8 * s >= a.n) break;
+            const uint32_t x = r0 + l + 8 * s;
             const uint32_t q = chunk_quot(a.cdiv, x);
             const uint32_t r = x - q * a.cdiv.d;
-            if (r == 0) a.chunk_off[t.q0 + q] = g;
-            const uint32_t e_lo = ent[k][2 * s], e_hi = ent[k][2 * s + 1];
+            if (r == 0) bnd[q] = g;
+            const uint32_t e_lo = kp.ent[2 * s], e_hi = kp.ent[2 * s + 1];
             if (miss_count(e_lo, e_hi)) {
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
-                    const uint32_t e = (j < 4 ? e_lo : e_hi) >> (8 * (j & 3));
-                    if (e & kMissEntry) {
-                        put_escape(a, g, r + j, (ex[k][2 * s + (j >> 2)] >> (8 * (j & 3))) & 0xFFu);
+                    if (((j < 4 ? e_lo : e_hi) >> (8 * (j & 3))) & kMissEntry) {
+                        lpos[g] = (uint16_t)(r + j);
+                        lval[g] = (uint8_t)(kp.ex[2 * s + (j >> 2)] >> (8 * (j & 3)));
                         g++;
                     }
                 }
             }
         }
     }
-    tile_finish(a, t, excl + aggregate);
+};
+
+// ------------------------------------------------------------------ roles
+
+// Lane 0 of the producer warp: claim tiles and fill the input ring.
+template <class F>
+__device__ void producer_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm) {
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+    uint32_t pending = 0, parity = 0;  // stages whose last arrival is a bulk copy, and its parity
+    for (uint32_t j = 0;; j++) {
+        const uint32_t s = j % kStages, use = j / kStages;
+        bool ok = wait_phase(&sm.empty[s], (use & 1) ^ 1);
+        if (!ok) record_timeout(a, sm);
+        const bool stop = !ok || *reinterpret_cast<volatile uint32_t*>(&sm.err);
+        const uint32_t tile = stop ? kInvalidTile : atomicAdd(&hdr->ticket, 1u);
+        if (tile >= a.num_tiles) {
+            sm.stage_tile[s] = kInvalidTile;
+            mbar_arrive(&sm.full[s]);
+            pending &= ~(1u << s);
+            break;
+        }
+        const uint32_t t0 = tile * (uint32_t)kTile;  // tile < num_tiles: t0 < n < 2^32
+        const uint32_t q0 = t0 / a.cdiv.d;
+        sm.stage_tile[s] = tile;
+        sm.stage_q0[s] = q0;
+        sm.stage_r0[s] = t0 - q0 * a.cdiv.d;
+        const uint32_t len = a.n - t0 < (uint32_t)kTile ? a.n - t0 : (uint32_t)kTile;
+        const uint32_t bytes = len * F::kElemBytes, b16 = bytes & ~15u;
+        const uint8_t* src = a.x + (uint64_t)t0 * F::kElemBytes;
+        for (uint32_t b = b16; b < bytes; b++) sm.stage[s][b] = src[b];  // < 16 tail bytes
+        if (b16) {
+            mbar_arrive_expect_tx(&sm.full[s], b16);
+            bulk_load(sm.stage[s], src, b16, &sm.full[s]);
+            pending |= 1u << s;
+            parity = (parity & ~(1u << s)) | ((use & 1) << s);
+        } else {
+            mbar_arrive(&sm.full[s]);
+            pending &= ~(1u << s);
+        }
+    }
+    // No bulk copy may still be writing this CTA's shared memory when it exits
+    // (on the normal path the compute warps have consumed every stage already).
+    for (uint32_t s = 0; s < kStages; s++)
+        if ((pending >> s) & 1u) wait_phase(&sm.full[s], (parity >> s) & 1u);
+}
+
+// The 8 compute warps.
+template <class F>
+__device__ void compute_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t j = 0;
+    for (;; j++) {
+        const uint32_t s = j % kStages, par = (j / kStages) & 1;
+        const uint32_t slot = j & 1, spar = ((j >> 1) & 1) ^ 1;
+        if (tid == 0) {
+            uint32_t t = kInvalidTile;
+            if (wait_phase(&sm.full[s], par)) t = sm.stage_tile[s];
+            else record_timeout(a, sm);
+            // The slot is needed either way: for this tile's escapes or for the end marker.
+            if (!wait_phase(&sm.slot_empty[slot], spar)) record_timeout(a, sm);
+            sm.cur_tile = t;
+        }
+        named_sync(1, kComputeThreads);
+        const uint32_t tile = sm.cur_tile;
+        if (tile == kInvalidTile) break;
+        mbar_try_wait(&sm.full[s], par);          // acquire the stage data in this thread
+        mbar_try_wait(&sm.slot_empty[slot], spar);  // and the slot's release by the look-back warp
+        const uint32_t t0 = tile * (uint32_t)kTile;
+        const uint32_t r0 = sm.stage_r0[s], q0 = sm.stage_q0[s];
+
+        typename F::Keep kp;
+        F::process(a, sm.stage[s], sm.table, t0, kp);
+        uint32_t rank[F::kGroups];
+        const uint32_t aggregate = block_ranks<F::kGroups>(kp.cnt, rank, sm.warp_tot[j & 1]);
+        // Past the scan's barrier every compute thread is done with stage s.
+        if (tid == 0) {
+            mbar_arrive(&sm.empty[s]);
+            sm.slot_tile[slot] = tile;
+            sm.slot_agg[slot] = aggregate;
+            sm.slot_q0[slot] = q0;
+            sm.slot_r0[slot] = r0;
+        }
+        F::emit(a, kp, rank, t0, r0, sm.list_pos[slot], sm.list_val[slot], sm.bnd[slot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.slot_full[slot]);
+    }
+    // End marker for the look-back warp (thread 0 already waited for the slot).
+    const uint32_t slot = j & 1;
+    if (tid == 0) sm.slot_tile[slot] = kInvalidTile;
+    if (lane == 0) mbar_arrive(&sm.slot_full[slot]);
+}
+
+// The look-back warp: global escape offsets, then escapes and chunk offsets.
+template <class F>
+__device__ void lookback_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm,
+                              uint32_t epoch) {
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+    const int lane = threadIdx.x & 31;
+    for (uint32_t j = 0;; j++) {
+        const uint32_t slot = j & 1, par = (j >> 1) & 1;
+        bool ok = lane == 0 ? wait_phase(&sm.slot_full[slot], par) : false;
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) {
+            if (lane == 0) record_timeout(a, sm);
+            break;
+        }
+        mbar_try_wait(&sm.slot_full[slot], par);
+        const uint32_t tile = sm.slot_tile[slot];
+        if (tile == kInvalidTile) break;
+        const uint32_t agg = min(sm.slot_agg[slot], (uint32_t)kTile);
+        const uint32_t q0 = sm.slot_q0[slot], r0 = sm.slot_r0[slot];
+        const uint32_t excl = look_back(a, tile, epoch, agg);
+        const uint16_t* lpos = sm.list_pos[slot];
+        const uint8_t* lval = sm.list_val[slot];
+        for (uint32_t r = lane; r < agg; r += 32) {
+            const uint32_t g = excl + r;
+            if ((uint64_t)g < a.esc_capacity) {
+                a.esc_pos[g] = lpos[r];
+                a.esc_val[g] = lval[r];
+            }
+        }
+        const uint32_t t0 = tile * (uint32_t)kTile;
+        const uint32_t len = a.n - t0 < (uint32_t)kTile ? a.n - t0 : (uint32_t)kTile;
+        const uint32_t qa = r0 ? 1u : 0u, qb = chunk_quot(a.cdiv, r0 + len - 1);
+        for (uint32_t q = qa + lane; q <= qb && q < (uint32_t)kMaxBoundaries; q += 32)
+            a.chunk_off[q0 + q] = excl + sm.bnd[slot][q];
+        if (tile == a.num_tiles - 1 && lane == 0) {
+            const uint32_t total = excl + agg;
+            a.chunk_off[a.nchunks] = total;
+            hdr->last_escapes = total;
+            if ((uint64_t)total > a.esc_capacity) atomicOr(&hdr->status, kStatusOverflow);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.slot_empty[slot]);
+    }
+}
+
+// Last CTA of the launch: move the status bits out and re-arm the header.  A
+// clean launch hands out exactly num_tiles + gridDim.x tickets (each producer
+// draws one past the end); anything else means the header did not start zeroed.
+__device__ void cta_finished(const EncodeArgs& a, uint32_t epoch, bool failed) {
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+    __threadfence();
+    const uint32_t prev = atomicAdd(&hdr->done, 1u);
+    if (prev == gridDim.x - 1) {
+        __threadfence();
+        const uint32_t tickets = atomicAdd(&hdr->ticket, 0u);
+        const bool timed_out = (atomicAdd(&hdr->status, 0u) & kStatusTimeout) != 0;
+        if (!failed && !timed_out && tickets != a.num_tiles + gridDim.x)
+            atomicOr(&hdr->status, kStatusBadWorkspace);
+        hdr->last_status = atomicExch(&hdr->status, 0u);
+        hdr->ticket = 0;
+        hdr->done = 0;
+        hdr->epoch = epoch + 1u;
+        __threadfence();
+    }
+}
+
+template <class F>
+__global__ void __launch_bounds__(kEncodeThreads, 2) encode_kernel(const EncodeArgs a) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    auto& sm = *reinterpret_cast<EncodeSmem<F::kElemBytes>*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    __shared__ uint32_t s_epoch;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int k = 0; k < 2; k++) {
+            mbar_init(&sm.slot_full[k], kComputeThreads / 32);
+            mbar_init(&sm.slot_empty[k], 1);
+        }
+        sm.err = 0;
+        s_epoch = *reinterpret_cast<volatile uint32_t*>(&reinterpret_cast<WsHeader*>(a.ws)->epoch);
+        fence_mbar_init();
+    }
+    if (tid < 256) sm.table[tid] = (uint8_t)kMissEntry;
+    __syncthreads();
+    if (tid < 16) sm.table[(a.cbw[tid >> 2] >> (8 * (tid & 3))) & 0xFFu] = (uint8_t)tid;
+    __syncthreads();
+    const uint32_t epoch = s_epoch;
+    if (warp < kComputeThreads / 32)
+        compute_role<F>(a, sm);
+    else if (warp == kComputeThreads / 32)
+        (tid & 31) == 0 ? producer_role<F>(a, sm) : (void)0;
+    else
+        lookback_role<F>(a, sm, epoch);
+    __syncthreads();
+    if (tid == 0) cta_finished(a, epoch, *reinterpret_cast<volatile uint32_t*>(&sm.err) != 0);
+}
+
+template <class F>
+cudaError_t launch_pipeline(const EncodeArgs& a, cudaStream_t s) {
+    constexpr size_t smem = sizeof(EncodeSmem<F::kElemBytes>);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(encode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<F>, kEncodeThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const uint32_t grid = min(a.num_tiles, (uint32_t)(sms * per_sm));
+    encode_kernel<F><<<grid, kEncodeThreads, smem, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-int encode_tile_elems(bool e5m2) { return e5m2 ? kE5m2Tile : kBf16Tile; }
+int encode_tile_elems(bool e5m2) { return (void)e5m2, kTile; }
 
 cudaError_t launch_encode(const EncodeArgs& a, bool e5m2, cudaStream_t s) {
     if (a.num_tiles == 0) return cudaSuccess;
-    if (e5m2)
-        encode_e5m2_kernel<<<a.num_tiles, kThreads, 0, s>>>(a);
-    else
-        encode_bf16_kernel<<<a.num_tiles, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return e5m2 ? launch_pipeline<E5m2Tile>(a, s) : launch_pipeline<Bf16Tile>(a, s);
 }
 
 }  // namespace splitzip

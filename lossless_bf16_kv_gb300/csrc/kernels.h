@@ -11,7 +11,7 @@ namespace splitzip {
 
 constexpr uint32_t kTestStallFirstTile = 1u;    // tile 0 never publishes (test hook)
 constexpr uint32_t kStatusBadWorkspace = 4u;    // a CTA drew a ticket past the grid
-constexpr uint32_t kDefaultSpinLimit = 1u << 23;  // polls of >= 100 ns: about a second
+constexpr uint32_t kDefaultSpinLimit = 1u << 21;  // look-back polls (load + 32 ns sleep): ~1 s
 
 struct EncodeArgs {
     const uint8_t* x;  // input bit patterns, 16-byte aligned
