@@ -84,66 +84,74 @@ __device__ __forceinline__ void split_e5m2(uint32_t w, uint32_t& ex, uint32_t& f
 
 // ------------------------------------------------------ decoupled look-back
 //
-// Run by all 32 lanes of the look-back warp.  Publishes the tile's aggregate,
-// then walks back over earlier tiles' state words until it meets an inclusive
+// Run by all 32 lanes of the look-back warp.  Walks back over earlier tiles' state words until it meets an inclusive
 // prefix, publishes this tile's inclusive prefix and returns the exclusive
-// one.  Each poll reads a window of 32 x kLookK predecessors (lane l reads the
-// kLookK words l*kLookK ... nearest first), because with every CTA working at
-// once a tile's nearest few hundred predecessors are often all in flight and
-// carry only aggregates.  Every wait is bounded by a.spin_limit polls.
+// one.  Each poll issues kLookK rows of 32 contiguous state words (row m,
+// lane l: predecessor 32m + l, nearest first) and consumes the rows in order,
+// because with every CTA working at once a tile's nearest few hundred
+// predecessors are often all in flight and carry only aggregates.  A poll
+// that finds a word not yet written backs off before the next one; every
+// wait is bounded by a.spin_limit polls.
 constexpr int kLookK = 8;
+
+// The tile's own word is published by the compute warps the moment its escape
+// count is known (publish_count below), so that later tiles' look-backs find
+// it as early as possible; this function only adds the inclusive prefix.
+__device__ __forceinline__ void publish_count(const EncodeArgs& a, uint32_t tile, uint32_t epoch,
+                                              uint32_t aggregate) {
+    uint64_t* states = reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes);
+    if (tile == 0) {
+        if (!(a.test_flags & kTestStallFirstTile))
+            st_relaxed_gpu(states, make_state(kFlagPrefix, aggregate, epoch));
+    } else {
+        st_relaxed_gpu(states + tile, make_state(kFlagAggregate, aggregate, epoch));
+    }
+}
 
 __device__ __forceinline__ uint32_t look_back(const EncodeArgs& a, uint32_t tile, uint32_t epoch,
                                               uint32_t aggregate) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     uint64_t* states = reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes);
     const int lane = threadIdx.x & 31;
-    if (tile == 0) {
-        if (lane == 0 && !(a.test_flags & kTestStallFirstTile))
-            st_relaxed_gpu(states, make_state(kFlagPrefix, aggregate, epoch));
-        return 0;
-    }
-    if (lane == 0) st_relaxed_gpu(states + tile, make_state(kFlagAggregate, aggregate, epoch));
-    uint32_t excl = 0, polls = 0;
+    if (tile == 0) return 0;
+    uint32_t excl = 0, polls = 0, backoff = 32;
     bool timed_out = false;
-    int64_t pred = (int64_t)tile - 1;
+    int64_t pred = (int64_t)tile - 1;  // nearest predecessor not yet summed
     while (true) {
         uint64_t w[kLookK];
 #pragma unroll
         for (int m = 0; m < kLookK; m++) {
-            const int64_t idx = pred - (lane * kLookK + m);
+            const int64_t idx = pred - (m * 32 + lane);
             w[m] = idx >= 0 ? ld_relaxed_gpu(states + idx) : make_state(kFlagPrefix, 0u, epoch);
         }
-        // This lane's words, nearest first: sum up to and including the first
-        // inclusive prefix; stop at a word that is not ready yet.
-        uint32_t sum = 0;
-        bool has_prefix = false, not_ready = false;
+        bool found = false, wait = false;
+        uint32_t rows = 0;
 #pragma unroll
         for (int m = 0; m < kLookK; m++) {
-            if (has_prefix || not_ready) continue;
+            if (found || wait) continue;  // warp-uniform
             const uint32_t f = state_flag(w[m], epoch);
-            if (f == 0u) {
-                not_ready = true;
-            } else {
-                sum += (uint32_t)w[m];
-                has_prefix = f == kFlagPrefix;
+            const uint32_t pm = __ballot_sync(0xFFFFFFFFu, f == kFlagPrefix);
+            const uint32_t bad = __ballot_sync(0xFFFFFFFFu, f == 0u);
+            // Lanes up to and including the nearest inclusive prefix (all 32 if none).
+            const uint32_t need = pm ? (((pm & (0u - pm)) << 1) - 1u) : 0xFFFFFFFFu;
+            if (bad & need) {
+                wait = true;
+                continue;
             }
+            excl += __reduce_add_sync(0xFFFFFFFFu, ((need >> lane) & 1u) ? (uint32_t)w[m] : 0u);
+            rows++;
+            found = pm != 0;
         }
-        const uint32_t pm = __ballot_sync(0xFFFFFFFFu, has_prefix);
-        const uint32_t bad = __ballot_sync(0xFFFFFFFFu, not_ready);
-        // Lanes up to and including the nearest lane with a prefix (all 32 if none).
-        const uint32_t need = pm ? (((pm & (0u - pm)) << 1) - 1u) : 0xFFFFFFFFu;
-        if (bad & need) {
+        if (found) break;
+        pred -= 32 * (int64_t)rows;
+        if (wait) {
             if (++polls > a.spin_limit) {
                 timed_out = true;
                 break;
             }
-            __nanosleep(32);
-            continue;
+            __nanosleep(backoff);
+            backoff = backoff < 256 ? backoff * 2 : 256;
         }
-        excl += __reduce_add_sync(0xFFFFFFFFu, ((need >> lane) & 1u) ? sum : 0u);
-        if (pm) break;
-        pred -= 32 * kLookK;
     }
     if (lane == 0) {
         if (timed_out) atomicOr(&hdr->status, kStatusTimeout);
@@ -156,29 +164,36 @@ __device__ __forceinline__ uint32_t look_back(const EncodeArgs& a, uint32_t tile
 // ------------------------------------------------------------ pipeline
 
 constexpr uint32_t kInvalidTile = 0xFFFFFFFFu;
-constexpr int kTile = 8192;                            // elements per tile, both formats
-constexpr int kStages = 3;                             // input ring depth
-constexpr int kComputeThreads = kThreads;              // 8 compute warps
-constexpr int kEncodeThreads = kComputeThreads + 64;   // + producer warp + look-back warp
-constexpr int kMaxBoundaries = kTile / 8 + 1;          // chunk starts one tile can hold
-constexpr uint64_t kWaitNs = 2000000000ull;            // an mbarrier wait gives up after 2 s
+constexpr int kTile = 8192;                      // elements per tile, both formats
+constexpr int kStages = 3;                       // input ring depth
+constexpr int kSlots = 8;                        // escape slots (compute -> look-back)
+constexpr int kLookbackWarps = 4;                // look-back warp w serves slots w, w + 4
+constexpr int kListCap = 1024;                   // escapes a slot holds; more: direct path
+constexpr int kComputeWarps = kThreads / 32;     // 8
+constexpr int kComputeThreads = kThreads;
+constexpr int kProducerWarp = kComputeWarps;     // warp 8
+constexpr int kEncodeThreads = kComputeThreads + 32 + 32 * kLookbackWarps;  // 416
+constexpr int kMaxBoundaries = kTile / 8 + 1;    // chunk starts one tile can hold
+constexpr uint64_t kWaitNs = 2000000000ull;      // an mbarrier wait gives up after 2 s
 
 template <int kElemBytes>
 struct EncodeSmem {
     alignas(128) uint8_t stage[kStages][kTile * kElemBytes];  // input ring (bulk-copy target)
-    uint16_t list_pos[2][kTile];    // escape slots: position in chunk, by rank in tile
-    uint8_t list_val[2][kTile];     //               raw exponent
-    uint32_t bnd[2][kMaxBoundaries];  // rank in tile at each chunk start, by chunk
-    uint8_t table[256];             // exponent -> code (kMissEntry: escape)
+    uint16_t list_pos[kSlots][kListCap];  // escapes by rank in tile: position in chunk
+    uint8_t list_val[kSlots][kListCap];   //                          raw exponent
+    uint16_t bnd[kSlots][kMaxBoundaries];  // rank in tile at each chunk start, by chunk
+    uint8_t table[256];                   // exponent -> code (kMissEntry: escape)
     uint32_t warp_tot[2][kWarps][2];
     uint32_t stage_tile[kStages], stage_q0[kStages], stage_r0[kStages];
-    uint32_t slot_tile[2], slot_agg[2], slot_q0[2], slot_r0[2];
-    uint32_t cur_tile;
+    uint32_t slot_tile[kSlots], slot_agg[kSlots], slot_q0[kSlots], slot_r0[kSlots];
+    uint32_t slot_excl[kSlots];           // direct path: the tile's global escape offset
+    uint32_t cur_tile, cur_excl;
     uint32_t err;
-    alignas(8) uint64_t full[kStages];   // producer -> compute: stage filled (tx bytes)
-    uint64_t empty[kStages];             // compute -> producer: stage consumed
-    uint64_t slot_full[2];               // compute -> look-back: slot filled (8 warps)
-    uint64_t slot_empty[2];              // look-back -> compute: slot written out
+    alignas(8) uint64_t full[kStages];    // producer -> compute: stage filled (tx bytes)
+    uint64_t empty[kStages];              // compute -> producer: stage consumed
+    uint64_t slot_full[kSlots];           // compute -> look-back: slot filled (8 warps)
+    uint64_t slot_empty[kSlots];          // look-back -> compute: slot written out
+    uint64_t slot_prefix[kSlots];         // look-back -> compute: offset of a direct tile
 };
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -253,6 +268,30 @@ __device__ __forceinline__ uint32_t block_ranks(const uint32_t (&c)[G], uint32_t
     return base;
 }
 
+// Where a tile's escapes go once ranked: into the slot's list (the look-back
+// warp copies them out), or straight to the escape stream at excl + rank.
+struct EscapeSink {
+    uint16_t* lpos;
+    uint8_t* lval;
+    uint16_t* gpos;
+    uint8_t* gval;
+    uint64_t cap;    // direct: escape capacity
+    uint32_t excl;   // direct: the tile's global offset
+    bool direct;
+    __device__ __forceinline__ void put(uint32_t rank, uint32_t pos, uint32_t e) const {
+        if (direct) {
+            const uint32_t g = excl + rank;
+            if ((uint64_t)g < cap) {
+                gpos[g] = (uint16_t)pos;
+                gval[g] = (uint8_t)e;
+            }
+        } else if (rank < (uint32_t)kListCap) {
+            lpos[rank] = (uint16_t)pos;
+            lval[rank] = (uint8_t)e;
+        }
+    }
+};
+
 // ------------------------------------------------------ per-format tiles
 //
 // BF16: thread t's groups of 8 sit at tile offsets k*2048 + 8t (k < 4), so a
@@ -311,30 +350,40 @@ struct Bf16Tile {
         }
     }
 
-    // Escapes into the slot at their ranks; ranks at chunk starts into bnd.
-    static __device__ __forceinline__ void emit(const EncodeArgs& a, const Keep& kp,
-                                                const uint32_t (&rank)[kGroups], uint32_t t0,
-                                                uint32_t r0, uint16_t* lpos, uint8_t* lval,
-                                                uint32_t* bnd) {
+    // Rank in tile at every chunk start this thread's groups hold.
+    static __device__ __forceinline__ void emit_bnd(const EncodeArgs& a, const Keep& kp,
+                                                    const uint32_t (&rank)[kGroups], uint32_t t0,
+                                                    uint32_t r0, uint16_t* bnd) {
         const bool full = (uint64_t)t0 + kTile <= a.n;
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
             const uint32_t l = loff(k);
             if (!full && t0 + l >= a.n) continue;
-            // A group of 8 lies inside one chunk (chunk % 8 == 0, group 8-aligned).
             const uint32_t x = r0 + l;
             const uint32_t q = chunk_quot(a.cdiv, x);
-            const uint32_t r = x - q * a.cdiv.d;
-            uint32_t g = rank[k];
-            if (r == 0) bnd[q] = g;
-            if (kp.cnt[k]) {
+            if (x == q * a.cdiv.d) bnd[q] = (uint16_t)rank[k];
+        }
+    }
+
+    // Escapes by rank; a group of 8 lies inside one chunk (chunk % 8 == 0).
+    static __device__ __forceinline__ void emit_escapes(const EncodeArgs& a, const Keep& kp,
+                                                        const uint32_t (&rank)[kGroups],
+                                                        uint32_t t0, uint32_t r0,
+                                                        const EscapeSink& sink) {
+        const bool full = (uint64_t)t0 + kTile <= a.n;
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    if ((kp.ent[k][j >> 2] >> (8 * (j & 3))) & kMissEntry) {
-                        lpos[g] = (uint16_t)(r + j);
-                        lval[g] = (uint8_t)(kp.ex[k][j >> 2] >> (8 * (j & 3)));
-                        g++;
-                    }
+        for (int k = 0; k < kGroups; k++) {
+            if (!kp.cnt[k]) continue;
+            const uint32_t l = loff(k);
+            if (!full && t0 + l >= a.n) continue;
+            const uint32_t x = r0 + l;
+            const uint32_t r = x - chunk_quot(a.cdiv, x) * a.cdiv.d;
+            uint32_t g = rank[k];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if ((kp.ent[k][j >> 2] >> (8 * (j & 3))) & kMissEntry) {
+                    sink.put(g, r + j, (kp.ex[k][j >> 2] >> (8 * (j & 3))) & 0xFFu);
+                    g++;
                 }
             }
         }
@@ -414,31 +463,43 @@ struct E5m2Tile {
         }
     }
 
-    static __device__ __forceinline__ void emit(const EncodeArgs& a, const Keep& kp,
-                                                const uint32_t (&rank)[kGroups], uint32_t t0,
-                                                uint32_t r0, uint16_t* lpos, uint8_t* lval,
-                                                uint32_t* bnd) {
+    // Four runs of 8 elements per group; each run lies inside one chunk.
+    static __device__ __forceinline__ void emit_bnd(const EncodeArgs& a, const Keep& kp,
+                                                    const uint32_t (&rank)[kGroups], uint32_t t0,
+                                                    uint32_t r0, uint16_t* bnd) {
         const bool full = (uint64_t)t0 + kTile <= a.n;
         const uint32_t l = loff();
-        if (!full && t0 + l >= a.n) return;
         uint32_t g = rank[0];
-        // Four runs of 8 elements; each lies inside one chunk.
 #pragma unroll
         for (int s = 0; s < 4; s++) {
             if (!full && t0 + l + 8 * s >= a.n) break;
             const uint32_t x = r0 + l + 8 * s;
             const uint32_t q = chunk_quot(a.cdiv, x);
-            const uint32_t r = x - q * a.cdiv.d;
-            if (r == 0) bnd[q] = g;
-            const uint32_t e_lo = kp.ent[2 * s], e_hi = kp.ent[2 * s + 1];
-            if (miss_count(e_lo, e_hi)) {
+            if (x == q * a.cdiv.d) bnd[q] = (uint16_t)g;
+            g += miss_count(kp.ent[2 * s], kp.ent[2 * s + 1]);
+        }
+    }
+
+    static __device__ __forceinline__ void emit_escapes(const EncodeArgs& a, const Keep& kp,
+                                                        const uint32_t (&rank)[kGroups],
+                                                        uint32_t t0, uint32_t r0,
+                                                        const EscapeSink& sink) {
+        if (!kp.cnt[0]) return;
+        const bool full = (uint64_t)t0 + kTile <= a.n;
+        const uint32_t l = loff();
+        uint32_t g = rank[0];
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    if (((j < 4 ? e_lo : e_hi) >> (8 * (j & 3))) & kMissEntry) {
-                        lpos[g] = (uint16_t)(r + j);
-                        lval[g] = (uint8_t)(kp.ex[2 * s + (j >> 2)] >> (8 * (j & 3)));
-                        g++;
-                    }
+        for (int s = 0; s < 4; s++) {
+            if (!full && t0 + l + 8 * s >= a.n) break;
+            const uint32_t e_lo = kp.ent[2 * s], e_hi = kp.ent[2 * s + 1];
+            if (!miss_count(e_lo, e_hi)) continue;
+            const uint32_t x = r0 + l + 8 * s;
+            const uint32_t r = x - chunk_quot(a.cdiv, x) * a.cdiv.d;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (((j < 4 ? e_lo : e_hi) >> (8 * (j & 3))) & kMissEntry) {
+                    sink.put(g, r + j, (kp.ex[2 * s + (j >> 2)] >> (8 * (j & 3))) & 0xFFu);
+                    g++;
                 }
             }
         }
@@ -491,25 +552,26 @@ __device__ void producer_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm
 
 // The 8 compute warps.
 template <class F>
-__device__ void compute_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm) {
+__device__ void compute_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm, uint32_t epoch) {
     const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t prefix_par = 0;  // bit k: parity of the next slot_prefix[k] phase
     uint32_t j = 0;
     for (;; j++) {
         const uint32_t s = j % kStages, par = (j / kStages) & 1;
-        const uint32_t slot = j & 1, spar = ((j >> 1) & 1) ^ 1;
+        const uint32_t k = j % kSlots, spar = ((j / kSlots) & 1) ^ 1;
         if (tid == 0) {
             uint32_t t = kInvalidTile;
             if (wait_phase(&sm.full[s], par)) t = sm.stage_tile[s];
             else record_timeout(a, sm);
-            // The slot is needed either way: for this tile's escapes or for the end marker.
-            if (!wait_phase(&sm.slot_empty[slot], spar)) record_timeout(a, sm);
+            // The slot is needed either way: for this tile or for an end marker.
+            if (!wait_phase(&sm.slot_empty[k], spar)) record_timeout(a, sm);
             sm.cur_tile = t;
         }
         named_sync(1, kComputeThreads);
         const uint32_t tile = sm.cur_tile;
         if (tile == kInvalidTile) break;
-        mbar_try_wait(&sm.full[s], par);          // acquire the stage data in this thread
-        mbar_try_wait(&sm.slot_empty[slot], spar);  // and the slot's release by the look-back warp
+        mbar_try_wait(&sm.full[s], par);        // acquire the stage data in this thread
+        mbar_try_wait(&sm.slot_empty[k], spar);  // and the slot's release by its look-back warp
         const uint32_t t0 = tile * (uint32_t)kTile;
         const uint32_t r0 = sm.stage_r0[s], q0 = sm.stage_q0[s];
 
@@ -517,58 +579,89 @@ __device__ void compute_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm)
         F::process(a, sm.stage[s], sm.table, t0, kp);
         uint32_t rank[F::kGroups];
         const uint32_t aggregate = block_ranks<F::kGroups>(kp.cnt, rank, sm.warp_tot[j & 1]);
+        const bool direct = aggregate > (uint32_t)kListCap;  // uniform
         // Past the scan's barrier every compute thread is done with stage s.
         if (tid == 0) {
+            publish_count(a, tile, epoch, aggregate);
             mbar_arrive(&sm.empty[s]);
-            sm.slot_tile[slot] = tile;
-            sm.slot_agg[slot] = aggregate;
-            sm.slot_q0[slot] = q0;
-            sm.slot_r0[slot] = r0;
+            sm.slot_tile[k] = tile;
+            sm.slot_agg[k] = aggregate;
+            sm.slot_q0[k] = q0;
+            sm.slot_r0[k] = r0;
         }
-        F::emit(a, kp, rank, t0, r0, sm.list_pos[slot], sm.list_val[slot], sm.bnd[slot]);
+        F::emit_bnd(a, kp, rank, t0, r0, sm.bnd[k]);
+        EscapeSink sink{sm.list_pos[k], sm.list_val[k], a.esc_pos, a.esc_val, a.esc_capacity, 0u,
+                        direct};
+        if (!direct) F::emit_escapes(a, kp, rank, t0, r0, sink);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.slot_full[slot]);
+        if (lane == 0) mbar_arrive(&sm.slot_full[k]);
+        if (direct) {
+            // Too many escapes for a slot: wait for this tile's offset and write
+            // them from registers.
+            if (tid == 0) {
+                if (!wait_phase(&sm.slot_prefix[k], (prefix_par >> k) & 1u)) record_timeout(a, sm);
+                sm.cur_excl = sm.slot_excl[k];
+            }
+            prefix_par ^= 1u << k;
+            named_sync(1, kComputeThreads);
+            sink.excl = sm.cur_excl;
+            F::emit_escapes(a, kp, rank, t0, r0, sink);
+        }
     }
-    // End marker for the look-back warp (thread 0 already waited for the slot).
-    const uint32_t slot = j & 1;
-    if (tid == 0) sm.slot_tile[slot] = kInvalidTile;
-    if (lane == 0) mbar_arrive(&sm.slot_full[slot]);
+    // End markers, one for each look-back warp (slot j was already waited for).
+    for (uint32_t m = 0; m < (uint32_t)kLookbackWarps; m++) {
+        const uint32_t jj = j + m, k = jj % kSlots, spar = ((jj / kSlots) & 1) ^ 1;
+        if (tid == 0) {
+            if (m > 0 && !wait_phase(&sm.slot_empty[k], spar)) record_timeout(a, sm);
+            sm.slot_tile[k] = kInvalidTile;
+        }
+        if (lane == 0) mbar_arrive(&sm.slot_full[k]);
+    }
 }
 
-// The look-back warp: global escape offsets, then escapes and chunk offsets.
+// Look-back warp lw: the tiles j = lw, lw + 4, ... of this CTA (slots lw and
+// lw + 4): global escape offset, escapes (unless direct) and chunk offsets.
 template <class F>
 __device__ void lookback_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm,
-                              uint32_t epoch) {
+                              uint32_t epoch, uint32_t lw) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     const int lane = threadIdx.x & 31;
-    for (uint32_t j = 0;; j++) {
-        const uint32_t slot = j & 1, par = (j >> 1) & 1;
-        bool ok = lane == 0 ? wait_phase(&sm.slot_full[slot], par) : false;
+    for (uint32_t j = lw;; j += kLookbackWarps) {
+        const uint32_t k = j % kSlots, par = (j / kSlots) & 1;
+        bool ok = lane == 0 ? wait_phase(&sm.slot_full[k], par) : false;
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) {
             if (lane == 0) record_timeout(a, sm);
             break;
         }
-        mbar_try_wait(&sm.slot_full[slot], par);
-        const uint32_t tile = sm.slot_tile[slot];
+        mbar_try_wait(&sm.slot_full[k], par);
+        const uint32_t tile = sm.slot_tile[k];
         if (tile == kInvalidTile) break;
-        const uint32_t agg = min(sm.slot_agg[slot], (uint32_t)kTile);
-        const uint32_t q0 = sm.slot_q0[slot], r0 = sm.slot_r0[slot];
+        const uint32_t agg = min(sm.slot_agg[k], (uint32_t)kTile);
+        const uint32_t q0 = sm.slot_q0[k], r0 = sm.slot_r0[k];
+        const bool direct = agg > (uint32_t)kListCap;
         const uint32_t excl = look_back(a, tile, epoch, agg);
-        const uint16_t* lpos = sm.list_pos[slot];
-        const uint8_t* lval = sm.list_val[slot];
-        for (uint32_t r = lane; r < agg; r += 32) {
-            const uint32_t g = excl + r;
-            if ((uint64_t)g < a.esc_capacity) {
-                a.esc_pos[g] = lpos[r];
-                a.esc_val[g] = lval[r];
+        if (direct) {
+            if (lane == 0) {
+                sm.slot_excl[k] = excl;
+                mbar_arrive(&sm.slot_prefix[k]);
+            }
+        } else {
+            const uint16_t* lpos = sm.list_pos[k];
+            const uint8_t* lval = sm.list_val[k];
+            for (uint32_t r = lane; r < agg; r += 32) {
+                const uint32_t g = excl + r;
+                if ((uint64_t)g < a.esc_capacity) {
+                    a.esc_pos[g] = lpos[r];
+                    a.esc_val[g] = lval[r];
+                }
             }
         }
         const uint32_t t0 = tile * (uint32_t)kTile;
         const uint32_t len = a.n - t0 < (uint32_t)kTile ? a.n - t0 : (uint32_t)kTile;
         const uint32_t qa = r0 ? 1u : 0u, qb = chunk_quot(a.cdiv, r0 + len - 1);
         for (uint32_t q = qa + lane; q <= qb && q < (uint32_t)kMaxBoundaries; q += 32)
-            a.chunk_off[q0 + q] = excl + sm.bnd[slot][q];
+            a.chunk_off[q0 + q] = excl + sm.bnd[k][q];
         if (tile == a.num_tiles - 1 && lane == 0) {
             const uint32_t total = excl + agg;
             a.chunk_off[a.nchunks] = total;
@@ -576,7 +669,7 @@ __device__ void lookback_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm
             if ((uint64_t)total > a.esc_capacity) atomicOr(&hdr->status, kStatusOverflow);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.slot_empty[slot]);
+        if (lane == 0) mbar_arrive(&sm.slot_empty[k]);
     }
 }
 
@@ -612,9 +705,10 @@ __global__ void __launch_bounds__(kEncodeThreads, 2) encode_kernel(const EncodeA
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
-        for (int k = 0; k < 2; k++) {
-            mbar_init(&sm.slot_full[k], kComputeThreads / 32);
+        for (int k = 0; k < kSlots; k++) {
+            mbar_init(&sm.slot_full[k], kComputeWarps);
             mbar_init(&sm.slot_empty[k], 1);
+            mbar_init(&sm.slot_prefix[k], 1);
         }
         sm.err = 0;
         s_epoch = *reinterpret_cast<volatile uint32_t*>(&reinterpret_cast<WsHeader*>(a.ws)->epoch);
@@ -625,12 +719,13 @@ __global__ void __launch_bounds__(kEncodeThreads, 2) encode_kernel(const EncodeA
     if (tid < 16) sm.table[(a.cbw[tid >> 2] >> (8 * (tid & 3))) & 0xFFu] = (uint8_t)tid;
     __syncthreads();
     const uint32_t epoch = s_epoch;
-    if (warp < kComputeThreads / 32)
-        compute_role<F>(a, sm);
-    else if (warp == kComputeThreads / 32)
-        (tid & 31) == 0 ? producer_role<F>(a, sm) : (void)0;
-    else
-        lookback_role<F>(a, sm, epoch);
+    if (warp < kComputeWarps) {
+        compute_role<F>(a, sm, epoch);
+    } else if (warp == kProducerWarp) {
+        if ((tid & 31) == 0) producer_role<F>(a, sm);
+    } else {
+        lookback_role<F>(a, sm, epoch, (uint32_t)(warp - kProducerWarp - 1));
+    }
     __syncthreads();
     if (tid == 0) cta_finished(a, epoch, *reinterpret_cast<volatile uint32_t*>(&sm.err) != 0);
 }
