@@ -90,17 +90,20 @@ __device__ __forceinline__ uint32_t ld_stream4(const void* p) {
     asm volatile("ld.global.cs.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
-// Streaming stores (written once, not re-read by this kernel).
+// Streaming stores (written once, never read back by the writing thread).
+// No "memory" clobber: the compiler may move this thread's other loads across
+// them (the streams are not re-read), while the asm volatile statements that
+// publish to other threads (mbarrier arrives, state-word stores) keep their
+// order relative to these stores.
 __device__ __forceinline__ void st_stream16(void* p, uint4 v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
+                 "r"(v.z), "r"(v.w));
 }
 __device__ __forceinline__ void st_stream8(void* p, uint2 v) {
-    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y));
 }
 __device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
-    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v));
 }
 
 // ------------------------------------------------------------- division

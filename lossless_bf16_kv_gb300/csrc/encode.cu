@@ -92,7 +92,7 @@ __device__ __forceinline__ void split_e5m2(uint32_t w, uint32_t& ex, uint32_t& f
 // predecessors are often all in flight and carry only aggregates.  A poll
 // that finds a word not yet written backs off before the next one; every
 // wait is bounded by a.spin_limit polls.
-constexpr int kLookK = 8;
+constexpr int kLookK = 4;
 
 // The tile's own word is published by the compute warps the moment its escape
 // count is known (publish_count below), so that later tiles' look-backs find
@@ -114,7 +114,7 @@ __device__ __forceinline__ uint32_t look_back(const EncodeArgs& a, uint32_t tile
     uint64_t* states = reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes);
     const int lane = threadIdx.x & 31;
     if (tile == 0) return 0;
-    uint32_t excl = 0, polls = 0, backoff = 32;
+    uint32_t excl = 0, polls = 0, backoff = 256;
     bool timed_out = false;
     int64_t pred = (int64_t)tile - 1;  // nearest predecessor not yet summed
     while (true) {
@@ -150,7 +150,7 @@ __device__ __forceinline__ uint32_t look_back(const EncodeArgs& a, uint32_t tile
                 break;
             }
             __nanosleep(backoff);
-            backoff = backoff < 256 ? backoff * 2 : 256;
+            backoff = backoff < 2048 ? backoff * 2 : 2048;
         }
     }
     if (lane == 0) {
@@ -203,13 +203,17 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Bounded wait on an mbarrier phase (time-based, so the bound does not depend
-// on how long a single try_wait suspends).
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+// on how long a single try_wait suspends).  Waits off the critical path pass
+// sleep_ns > 0 so that their polling does not take issue slots from the
+// compute warps.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        for (int i = 0; i < 64; i++)
+        for (int i = 0; i < 16; i++) {
+            if (sleep_ns) __nanosleep(sleep_ns);
             if (mbar_try_wait(bar, parity)) return true;
+        }
         if (global_ns() - t0 > kWaitNs) return false;
     }
 }
@@ -310,15 +314,39 @@ struct Bf16Tile {
     static __device__ __forceinline__ void process(const EncodeArgs& a, const uint8_t* stage,
                                                    const uint8_t* table, uint32_t t0, Keep& kp) {
         const bool full = (uint64_t)t0 + kTile <= a.n;
+        if (full) {
+            // Whole tile: every group's stage reads and table lookups first,
+            // then the stores, so that the lookups of all groups overlap.
+            uint32_t sm[kGroups][2];
+#pragma unroll
+            for (int k = 0; k < kGroups; k++) {
+                const uint4 v = *reinterpret_cast<const uint4*>(stage + 2 * loff(k));
+                split_bf16(v.x, v.y, sm[k][0], kp.ex[k][0]);
+                split_bf16(v.z, v.w, sm[k][1], kp.ex[k][1]);
+            }
+#pragma unroll
+            for (int k = 0; k < kGroups; k++) {
+                kp.ent[k][0] = lookup4(table, kp.ex[k][0]);
+                kp.ent[k][1] = lookup4(table, kp.ex[k][1]);
+            }
+#pragma unroll
+            for (int k = 0; k < kGroups; k++) {
+                const uint32_t i = t0 + loff(k);
+                kp.cnt[k] = miss_count(kp.ent[k][0], kp.ent[k][1]);
+                st_stream4(a.codes + i / 2, pack_nibbles(kp.ent[k][0], kp.ent[k][1]));
+                st_stream8(a.signman + i, make_uint2(sm[k][0], sm[k][1]));
+            }
+            return;
+        }
         const uint32_t pad = (a.cbw[0] & 0xFFu) << 7;  // exponent cb[0], sign 0, mantissa 0: code 0
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
             const uint32_t l = loff(k), i = t0 + l;
             kp.cnt[k] = 0;
             kp.ent[k][0] = kp.ent[k][1] = 0;
-            if (!full && i >= a.n) continue;
+            if (i >= a.n) continue;
             uint4 v;
-            const bool whole = full || i + 8 <= a.n;
+            const bool whole = i + 8 <= a.n;
             if (whole) {
                 v = *reinterpret_cast<const uint4*>(stage + 2 * l);
             } else {
@@ -515,7 +543,7 @@ __device__ void producer_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm
     uint32_t pending = 0, parity = 0;  // stages whose last arrival is a bulk copy, and its parity
     for (uint32_t j = 0;; j++) {
         const uint32_t s = j % kStages, use = j / kStages;
-        bool ok = wait_phase(&sm.empty[s], (use & 1) ^ 1);
+        bool ok = wait_phase(&sm.empty[s], (use & 1) ^ 1, 128);
         if (!ok) record_timeout(a, sm);
         const bool stop = !ok || *reinterpret_cast<volatile uint32_t*>(&sm.err);
         const uint32_t tile = stop ? kInvalidTile : atomicAdd(&hdr->ticket, 1u);
@@ -628,7 +656,7 @@ __device__ void lookback_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm
     const int lane = threadIdx.x & 31;
     for (uint32_t j = lw;; j += kLookbackWarps) {
         const uint32_t k = j % kSlots, par = (j / kSlots) & 1;
-        bool ok = lane == 0 ? wait_phase(&sm.slot_full[k], par) : false;
+        bool ok = lane == 0 ? wait_phase(&sm.slot_full[k], par, 256) : false;
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) {
             if (lane == 0) record_timeout(a, sm);
