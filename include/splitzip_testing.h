@@ -2,9 +2,10 @@
  * splitzip_testing.h -- test controls of the SplitZip library (not for
  * production callers).
  *
- * The encode kernel computes the exclusive prefix of escape counts across
- * tiles with a decoupled look-back: a tile waits until its predecessors have
- * published their counts.  Every such wait is bounded; when the bound runs
+ * Both encode engines compute the exclusive prefix of escape counts across
+ * tiles with a decoupled look-back (per 8192-element tile in the single-launch
+ * pipeline, per block of 2048 tiles in the three-launch encode): a tile waits
+ * until its predecessors have published their counts.  Every such wait is bounded; when the bound runs
  * out the kernel records SPLITZIP_ERR_TIMEOUT in the workspace, publishes a
  * (wrong) prefix so that later tiles are not held up, keeps every write in
  * bounds and returns, leaving the CUDA context usable.  This entry point lets
@@ -24,6 +25,9 @@ extern "C" {
 
 /* Tile 0 never publishes its prefix: every later tile's wait runs out. */
 #define SPLITZIP_TEST_STALL_FIRST_TILE 0x1u
+/* Encode with the single-launch pipeline (the engine of
+ * splitzip_encode_noalloc) instead of the three-launch encode. */
+#define SPLITZIP_TEST_PIPELINED 0x2u
 
 typedef struct splitzip_encode_test_opts {
     uint32_t spin_limit;  /* polls (about 100 ns apart) before a wait gives up; 0 = default */

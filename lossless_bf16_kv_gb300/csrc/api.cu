@@ -86,7 +86,8 @@ splitzip_status encode_impl(const void* d_x, uint64_t n, uint32_t chunk,
     a.spin_limit = spin_limit ? spin_limit : kDefaultSpinLimit;
     a.test_flags = flags;
     pack_codebook(cb, a.cbw);
-    return from_cuda(launch_encode(a, e5m2, s));
+    return from_cuda((flags & kTestPipelined) ? launch_encode(a, e5m2, s)
+                                              : launch_encode_multi(a, e5m2, s));
 }
 
 splitzip_status decode_impl(const splitzip_streams* in, uint64_t n, uint32_t chunk,
@@ -158,9 +159,7 @@ extern "C" {
 
 size_t splitzip_workspace_bytes(uint64_t n, uint32_t chunk_size) {
     (void)chunk_size;
-    // BF16 tiles are the smaller ones, so they bound the tile count.
-    const uint64_t tiles = ceil_div(n ? n : 1, (uint64_t)encode_tile_elems(false));
-    return kWsHeaderBytes + 8 * tiles;
+    return multi_layout(n).bytes;
 }
 
 splitzip_status splitzip_workspace_init(void* d_workspace, size_t bytes, splitzip_stream_t s) {
@@ -227,7 +226,8 @@ splitzip_status splitzip_encode_test(const void* d_x, uint64_t n, uint32_t chunk
                                      void* d_workspace, splitzip_stream_t s, int is_e5m2,
                                      const splitzip_encode_test_opts* opts) {
     const uint32_t limit = opts ? opts->spin_limit : 0;
-    const uint32_t flags = opts ? (opts->flags & SPLITZIP_TEST_STALL_FIRST_TILE) : 0;
+    const uint32_t flags =
+        opts ? (opts->flags & (SPLITZIP_TEST_STALL_FIRST_TILE | SPLITZIP_TEST_PIPELINED)) : 0;
     return encode_impl(d_x, n, chunk_size, cb, out, d_workspace, (cudaStream_t)s, is_e5m2 != 0,
                        limit, flags);
 }

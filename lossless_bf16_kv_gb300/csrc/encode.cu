@@ -31,135 +31,12 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "fields.cuh"
+#include "lookback.cuh"
 #include "kernels.h"
 
 namespace splitzip {
 namespace {
-
-constexpr uint32_t kMissEntry = 0x10u;  // table entry of an exponent outside the codebook
-
-// Four table entries for the four exponent bytes of `ex`, one per byte.
-__device__ __forceinline__ uint32_t lookup4(const uint8_t* table, uint32_t ex) {
-    const uint32_t e0 = table[ex & 0xFFu];
-    const uint32_t e1 = table[(ex >> 8) & 0xFFu];
-    const uint32_t e2 = table[(ex >> 16) & 0xFFu];
-    const uint32_t e3 = table[ex >> 24];
-    return __byte_perm(__byte_perm(e0, e1, 0x0040), __byte_perm(e2, e3, 0x0040), 0x5410);
-}
-
-// Packs the codes of two entry words (elements 0..3 and 4..7) into 8 nibbles:
-// byte j holds elements 2j (low nibble) and 2j+1 (high nibble).
-__device__ __forceinline__ uint32_t pack_nibbles(uint32_t w_lo, uint32_t w_hi) {
-    const uint32_t p_lo = (w_lo & 0x0F0F0F0Fu) | ((w_lo >> 4) & 0xF0F0F0F0u);
-    const uint32_t p_hi = (w_hi & 0x0F0F0F0Fu) | ((w_hi >> 4) & 0xF0F0F0F0u);
-    return __byte_perm(p_lo, p_hi, 0x6420);
-}
-
-__device__ __forceinline__ uint32_t miss_count(uint32_t w_lo, uint32_t w_hi) {
-    return __popc((w_lo & 0x10101010u) | ((w_hi & 0x10101010u) >> 1));
-}
-
-// ------------------------------------------------------------------- BF16
-//
-// Field split of 8 BF16 values (4 words, 2 values each): the low bytes of
-// elements 0..3 gather into one word and the high bytes into another, so the
-// sign+mantissa byte (sign from the high byte's bit 7, mantissa from the low
-// byte's bits 0..6) and the exponent byte (high byte bits 0..6 above low byte
-// bit 7) come out four at a time.
-__device__ __forceinline__ void split_bf16(uint32_t a, uint32_t b, uint32_t& sm, uint32_t& ex) {
-    const uint32_t lo = __byte_perm(a, b, 0x6420);
-    const uint32_t hi = __byte_perm(a, b, 0x7531);
-    sm = (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
-    ex = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
-}
-
-// 4 E5M2 bytes -> 4 exponent bytes and 4 three-bit fields packed in 12 bits
-// (field of byte k at bits 3k..3k+2).
-__device__ __forceinline__ void split_e5m2(uint32_t w, uint32_t& ex, uint32_t& f12) {
-    ex = (w >> 2) & 0x1F1F1F1Fu;
-    const uint32_t f = ((w >> 5) & 0x04040404u) | (w & 0x03030303u);  // sign<<2 | mantissa
-    const uint32_t t = f | (f >> 5);
-    f12 = (t & 0x3Fu) | ((t >> 10) & 0xFC0u);
-}
-
-// ------------------------------------------------------ decoupled look-back
-//
-// Run by all 32 lanes of the look-back warp.  Walks back over earlier tiles' state words until it meets an inclusive
-// prefix, publishes this tile's inclusive prefix and returns the exclusive
-// one.  Each poll issues kLookK rows of 32 contiguous state words (row m,
-// lane l: predecessor 32m + l, nearest first) and consumes the rows in order,
-// because with every CTA working at once a tile's nearest few hundred
-// predecessors are often all in flight and carry only aggregates.  A poll
-// that finds a word not yet written backs off before the next one; every
-// wait is bounded by a.spin_limit polls.
-constexpr int kLookK = 4;
-
-// The tile's own word is published by the compute warps the moment its escape
-// count is known (publish_count below), so that later tiles' look-backs find
-// it as early as possible; this function only adds the inclusive prefix.
-__device__ __forceinline__ void publish_count(const EncodeArgs& a, uint32_t tile, uint32_t epoch,
-                                              uint32_t aggregate) {
-    uint64_t* states = reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes);
-    if (tile == 0) {
-        if (!(a.test_flags & kTestStallFirstTile))
-            st_relaxed_gpu(states, make_state(kFlagPrefix, aggregate, epoch));
-    } else {
-        st_relaxed_gpu(states + tile, make_state(kFlagAggregate, aggregate, epoch));
-    }
-}
-
-__device__ __forceinline__ uint32_t look_back(const EncodeArgs& a, uint32_t tile, uint32_t epoch,
-                                              uint32_t aggregate) {
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
-    uint64_t* states = reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes);
-    const int lane = threadIdx.x & 31;
-    if (tile == 0) return 0;
-    uint32_t excl = 0, polls = 0, backoff = 256;
-    bool timed_out = false;
-    int64_t pred = (int64_t)tile - 1;  // nearest predecessor not yet summed
-    while (true) {
-        uint64_t w[kLookK];
-#pragma unroll
-        for (int m = 0; m < kLookK; m++) {
-            const int64_t idx = pred - (m * 32 + lane);
-            w[m] = idx >= 0 ? ld_relaxed_gpu(states + idx) : make_state(kFlagPrefix, 0u, epoch);
-        }
-        bool found = false, wait = false;
-        uint32_t rows = 0;
-#pragma unroll
-        for (int m = 0; m < kLookK; m++) {
-            if (found || wait) continue;  // warp-uniform
-            const uint32_t f = state_flag(w[m], epoch);
-            const uint32_t pm = __ballot_sync(0xFFFFFFFFu, f == kFlagPrefix);
-            const uint32_t bad = __ballot_sync(0xFFFFFFFFu, f == 0u);
-            // Lanes up to and including the nearest inclusive prefix (all 32 if none).
-            const uint32_t need = pm ? (((pm & (0u - pm)) << 1) - 1u) : 0xFFFFFFFFu;
-            if (bad & need) {
-                wait = true;
-                continue;
-            }
-            excl += __reduce_add_sync(0xFFFFFFFFu, ((need >> lane) & 1u) ? (uint32_t)w[m] : 0u);
-            rows++;
-            found = pm != 0;
-        }
-        if (found) break;
-        pred -= 32 * (int64_t)rows;
-        if (wait) {
-            if (++polls > a.spin_limit) {
-                timed_out = true;
-                break;
-            }
-            __nanosleep(backoff);
-            backoff = backoff < 2048 ? backoff * 2 : 2048;
-        }
-    }
-    if (lane == 0) {
-        if (timed_out) atomicOr(&hdr->status, kStatusTimeout);
-        // Published even after a time-out so that later tiles are not held up.
-        st_relaxed_gpu(states + tile, make_state(kFlagPrefix, excl + aggregate, epoch));
-    }
-    return excl;
-}
 
 // ------------------------------------------------------------ pipeline
 
@@ -610,7 +487,8 @@ __device__ void compute_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm,
         const bool direct = aggregate > (uint32_t)kListCap;  // uniform
         // Past the scan's barrier every compute thread is done with stage s.
         if (tid == 0) {
-            publish_count(a, tile, epoch, aggregate);
+            publish_count(reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes), tile, epoch, aggregate,
+                          (a.test_flags & kTestStallFirstTile) != 0);
             mbar_arrive(&sm.empty[s]);
             sm.slot_tile[k] = tile;
             sm.slot_agg[k] = aggregate;
@@ -668,7 +546,9 @@ __device__ void lookback_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm
         const uint32_t agg = min(sm.slot_agg[k], (uint32_t)kTile);
         const uint32_t q0 = sm.slot_q0[k], r0 = sm.slot_r0[k];
         const bool direct = agg > (uint32_t)kListCap;
-        const uint32_t excl = look_back(a, tile, epoch, agg);
+        const uint32_t excl = look_back(reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes),
+                                        &reinterpret_cast<WsHeader*>(a.ws)->status, tile, epoch, agg,
+                                        a.spin_limit);
         if (direct) {
             if (lane == 0) {
                 sm.slot_excl[k] = excl;

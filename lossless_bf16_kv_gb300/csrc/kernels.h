@@ -10,6 +10,7 @@
 namespace splitzip {
 
 constexpr uint32_t kTestStallFirstTile = 1u;    // tile 0 never publishes (test hook)
+constexpr uint32_t kTestPipelined = 2u;         // test hook: run the single-launch pipeline
 constexpr uint32_t kStatusBadWorkspace = 4u;    // a CTA drew a ticket past the grid
 constexpr uint32_t kDefaultSpinLimit = 1u << 21;  // look-back polls (load + 32 ns sleep): ~1 s
 
@@ -55,9 +56,26 @@ struct CalibArgs {
     uint64_t* covered_out;  // device
 };
 
+// Workspace layout of the multi-kernel encode, all offsets from the workspace
+// start (256-byte aligned):
+//   [0, 4096)            header (WsHeader)
+//   states               8 bytes per tile: look-back state words (the single-
+//                        launch pipeline uses one per tile, the tile-prefix
+//                        kernel one per 2048 tiles)
+//   tile_total, tile_excl  4 bytes per tile: escapes per tile and their
+//                        exclusive prefix
+//   seg_cnt              32 x uint16 per tile: escapes per segment
+//   seg_ent              256 x uint16 per tile: the segments' first escapes
+//                        (position in segment | exponent << offset bits)
+struct MultiLayout {
+    size_t states, tile_total, tile_excl, seg_cnt, seg_ent, bytes;
+};
+MultiLayout multi_layout(uint64_t n);
+
 int encode_tile_elems(bool e5m2);
 int decode_tile_elems(bool e5m2);
-cudaError_t launch_encode(const EncodeArgs& a, bool e5m2, cudaStream_t s);
+cudaError_t launch_encode(const EncodeArgs& a, bool e5m2, cudaStream_t s);        // one launch
+cudaError_t launch_encode_multi(const EncodeArgs& a, bool e5m2, cudaStream_t s);  // three launches
 cudaError_t launch_decode(const DecodeArgs& a, bool e5m2, cudaStream_t s);
 cudaError_t launch_calibrate(const CalibArgs& a, bool e5m2, cudaStream_t s);
 uint32_t calibrate_grid(uint32_t n, int num_sms);

@@ -29,6 +29,7 @@ STATUS_NAMES = {OK: "OK", ERR_INVALID_ARG: "INVALID_ARG", ERR_ESCAPE_OVERFLOW: "
 MAX_CHUNK = 65536
 MAX_ELEMENTS = 0xFFFFFFFF
 TEST_STALL_FIRST_TILE = 0x1
+TEST_PIPELINED = 0x2
 
 
 class SplitZipError(RuntimeError):

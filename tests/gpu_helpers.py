@@ -37,8 +37,12 @@ def gpu_calibrate(x: torch.Tensor):
     return sz.splitzip_calibrate(flat, ws, fmt_of(x))
 
 
-def gpu_encode(x: torch.Tensor, chunk: int, cb, esc_capacity=None, ws=None):
-    """Encode on the GPU; returns (host streams dict, status, E, device streams)."""
+def gpu_encode(x: torch.Tensor, chunk: int, cb, esc_capacity=None, ws=None, engine="multi"):
+    """Encode on the GPU; returns (host streams dict, status, E, device streams).
+
+    engine "multi" is splitzip_encode (three launches); "pipelined" is the
+    single-launch pipeline behind splitzip_encode_noalloc, reached through the
+    test entry point."""
     ensure_library()
     flat = x.reshape(-1)
     n = flat.numel()
@@ -46,7 +50,10 @@ def gpu_encode(x: torch.Tensor, chunk: int, cb, esc_capacity=None, ws=None):
     if ws is None:
         ws = sz.alloc_workspace(n, flat.device)
     st = sz.alloc_streams(n, chunk, fmt, esc_capacity, flat.device)
-    sz.splitzip_encode(flat, chunk, cb, st, ws, fmt)
+    if engine == "pipelined":
+        sz.splitzip_encode_test(flat, chunk, cb, st, ws, fmt, flags=sz.TEST_PIPELINED)
+    else:
+        sz.splitzip_encode(flat, chunk, cb, st, ws, fmt)
     status, E = sz.splitzip_encode_status(ws)
     stored = min(E, st["esc_pos"].numel())
     host = {

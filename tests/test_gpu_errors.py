@@ -79,21 +79,23 @@ def test_escape_overflow(fmt):
     assert_streams_equal(again, ref, "after overflow")
 
 
+@pytest.mark.parametrize("engine", ["multi", "pipelined"])
 @pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
-def test_lookback_wait_gives_up(fmt):
-    """Tile 0 never publishes its prefix; tile 1 polls 2000 times (~0.2 ms),
+def test_lookback_wait_gives_up(fmt, engine):
+    """The first tile (pipelined) or first block of 2048 tiles (three-launch
+    encode) never publishes its prefix; its successor polls 2000 times,
     records TIMEOUT and returns.  The context stays usable."""
-    x, cb = _setup(n=40_000, fmt=fmt)
-    n = x.numel()
+    n = 40_000 if engine == "pipelined" else 2048 * 8192 + 100
+    x, cb = _setup(n=n, fmt=fmt)
     ws = sz.alloc_workspace(n, DEV)
     st = sz.alloc_streams(n, 1024, fmt, esc_capacity=n)
-    sz.splitzip_encode_test(x, 1024, cb, st, ws, fmt, spin_limit=2000,
-                            flags=sz.TEST_STALL_FIRST_TILE)
+    flags = sz.TEST_STALL_FIRST_TILE | (sz.TEST_PIPELINED if engine == "pipelined" else 0)
+    sz.splitzip_encode_test(x, 1024, cb, st, ws, fmt, spin_limit=2000, flags=flags)
     status, _ = sz.splitzip_encode_status(ws)
     assert status == sz.ERR_TIMEOUT
     # Same workspace, normal call: correct again.
     ref = oracle.encode(host_bits(x), 1024, np.asarray(cb, np.uint8), fmt)
-    gpu, status, _, _ = gpu_encode(x, 1024, cb, esc_capacity=n, ws=ws)
+    gpu, status, _, _ = gpu_encode(x, 1024, cb, esc_capacity=n, ws=ws, engine=engine)
     assert status == sz.OK
     assert_streams_equal(gpu, ref, "after timeout")
 

@@ -121,6 +121,28 @@ def test_deterministic_and_workspace_reuse():
             assert_streams_equal(again, ref, "repeat")
 
 
+# ------------------------------------------- the single-launch engine
+
+@pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
+def test_pipelined_engine_matches_oracle(fmt):
+    """The single-launch pipeline (engine of splitzip_encode_noalloc) gives the
+    oracle's streams too, on ragged sizes, small and large chunks, and an
+    escape-dense input (tiles beyond its escape slots take the direct path)."""
+    dt = torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2
+    cal = synth.kv_cache(1, 8, seed=1, device=DEV, dtype=dt)
+    cb, _ = gpu_calibrate(cal)
+    inputs = [synth.kv_cache(1, 777, seed=3, device=DEV, dtype=dt).reshape(-1)[:1_500_007],
+              synth.student_t_scaled_bf16((300_001,), seed=7, device=DEV).float().to(dt)]
+    for x in inputs:
+        xb = host_bits(x)
+        for chunk in (8, 24, 1024, 65536):
+            ref = oracle.encode(xb, chunk, np.asarray(cb, np.uint8), fmt)
+            gpu, status, _, _ = gpu_encode(x, chunk, cb, esc_capacity=ref["n_escapes"] + 16,
+                                           engine="pipelined")
+            assert status == 0
+            assert_streams_equal(gpu, ref, f"pipelined {fmt} n={x.numel()} chunk {chunk}")
+
+
 # ------------------------------------------------ full-size configurations
 
 @pytest.mark.parametrize("name", ["kv_prefill_64L_16k", "kv_prefill_64L_16k_e5m2"])
