@@ -92,8 +92,8 @@ typedef struct splitzip_streams {
 /* ---------------------------------------------------------------- sizes */
 
 /* Bytes of device workspace needed by calibrate/encode for n elements, about
- * 0.07 bytes per element (per 8192-element tile: a look-back word, two
- * counters, 32 segment counts and 256 escape entries; independent of the
+ * 0.07 bytes per element (per 8192-element tile: a look-back word, a
+ * prefix, 32 segment counts and 256 escape entries; independent of the
  * chunk size today -- the argument is kept for later formats).  The workspace
  * must be zero-filled once after allocation (splitzip_workspace_init); the
  * library keeps it consistent afterwards. */

@@ -14,8 +14,9 @@
 //                dense code and sign+mantissa stores.  Each warp ranks the
 //                escapes of its segments with shuffles and stores the count
 //                and the first few escapes of every segment in the
-//                workspace, plus the tile's escape count.
-//   K2 prefix    exclusive prefix of the per-tile counts (2048 tiles per CTA,
+//                workspace.
+//   K2 prefix    exclusive prefix of the per-tile escape counts (sums of the
+//                segment counts; 2048 tiles per CTA,
 //                decoupled look-back across CTAs, bounded waits); E.
 //   K3 place     a warp per tile: segment offsets by shuffle scan, escapes
 //                copied to their final places, chunk offsets at chunk starts.
@@ -44,7 +45,6 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct MultiPtrs {
     uint64_t* states;
-    uint32_t* tile_total;
     uint32_t* tile_excl;
     uint16_t* seg_cnt;
     uint16_t* seg_ent;
@@ -305,30 +305,25 @@ struct E5m2Dense {
 
 // --------------------------------------------------------------- K1 dense
 
+// Grid-stride over tiles (one resident wave): the code table is built once
+// per CTA and the tile loop has no barrier at all.
 template <class F>
 __global__ void __launch_bounds__(kThreads) dense_kernel(const EncodeArgs a, const MultiPtrs p) {
     constexpr int G = F::kGroups;
     __shared__ uint8_t table[256];
-    __shared__ uint32_t s_total;
-    if (threadIdx.x == 0) s_total = 0;
     build_table(table, a.cbw);
-    const uint32_t tile = blockIdx.x, t0 = tile * (uint32_t)kTileElems;
     const uint32_t lane = threadIdx.x & 31;
-
-    typename F::Keep kp;
-    F::process(a, table, t0, kp);
-    uint32_t rel[G], tot[G];
-    warp_scan<G>(kp.cnt, rel, tot);
-    uint32_t wsum = 0;
+    for (uint32_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+        const uint32_t t0 = tile * (uint32_t)kTileElems;
+        typename F::Keep kp;
+        F::process(a, table, t0, kp);
+        uint32_t rel[G], tot[G];
+        warp_scan<G>(kp.cnt, rel, tot);
 #pragma unroll
-    for (int g = 0; g < G; g++) {
-        wsum += tot[g];
-        if (lane == (uint32_t)g) p.seg_cnt[(size_t)tile * kSegsMax + F::seg(g)] = (uint16_t)tot[g];
+        for (int g = 0; g < G; g++)
+            if (lane == (uint32_t)g) p.seg_cnt[(size_t)tile * kSegsMax + F::seg(g)] = (uint16_t)tot[g];
+        F::emit(kp, rel, p.seg_ent + (size_t)tile * kEntries);
     }
-    F::emit(kp, rel, p.seg_ent + (size_t)tile * kEntries);
-    if (lane == 0 && wsum) atomicAdd(&s_total, wsum);
-    __syncthreads();
-    if (threadIdx.x == 0) p.tile_total[tile] = s_total;
 }
 
 // -------------------------------------------------------------- K2 prefix
@@ -354,7 +349,8 @@ __device__ void prefix_finished(const EncodeArgs& a, uint32_t epoch) {
 }
 
 __global__ void __launch_bounds__(kThreads) prefix_kernel(const EncodeArgs a, const MultiPtrs p,
-                                                          uint32_t num_tiles, uint32_t num_blocks) {
+                                                          uint32_t num_tiles, uint32_t num_blocks,
+                                                          uint32_t segs) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     __shared__ uint32_t s_blk, s_epoch, s_excl;
     __shared__ uint32_t s_warp[kWarps];
@@ -372,16 +368,23 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const EncodeArgs a, co
         }
         return;
     }
+    // Tile totals: the sum of each tile's segment counts (16-bit, 32 per tile,
+    // the first `segs` in use).
     const uint32_t base = blk * (uint32_t)kScanTiles + tid * 8;
     uint32_t v[8];
-    if (base + 8 <= num_tiles) {
-        const uint4 lo = *reinterpret_cast<const uint4*>(p.tile_total + base);
-        const uint4 hi = *reinterpret_cast<const uint4*>(p.tile_total + base + 4);
-        v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
-        v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
-    } else {
 #pragma unroll
-        for (int i = 0; i < 8; i++) v[i] = base + i < num_tiles ? p.tile_total[base + i] : 0u;
+    for (int i = 0; i < 8; i++) {
+        v[i] = 0;
+        if (base + i >= num_tiles) continue;
+        const uint4* row = reinterpret_cast<const uint4*>(p.seg_cnt + (size_t)(base + i) * kSegsMax);
+#pragma unroll
+        for (int q = 0; q < kSegsMax / 8; q++) {
+            if ((uint32_t)q * 8 >= segs) break;
+            const uint4 c = row[q];
+            const uint32_t w = (c.x & 0xFFFFu) + (c.x >> 16) + (c.y & 0xFFFFu) + (c.y >> 16) +
+                               (c.z & 0xFFFFu) + (c.z >> 16) + (c.w & 0xFFFFu) + (c.w >> 16);
+            v[i] += w;
+        }
     }
     uint32_t sum = 0;
 #pragma unroll
@@ -510,16 +513,22 @@ cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
     const MultiLayout L = multi_layout(a.n);
     MultiPtrs p;
     p.states = reinterpret_cast<uint64_t*>(a.ws + L.states);
-    p.tile_total = reinterpret_cast<uint32_t*>(a.ws + L.tile_total);
     p.tile_excl = reinterpret_cast<uint32_t*>(a.ws + L.tile_excl);
     p.seg_cnt = reinterpret_cast<uint16_t*>(a.ws + L.seg_cnt);
     p.seg_ent = reinterpret_cast<uint16_t*>(a.ws + L.seg_ent);
     const uint32_t tiles = a.num_tiles;
     const uint32_t blocks = (tiles + kScanTiles - 1) / kScanTiles;
-    dense_kernel<F><<<tiles, kThreads, 0, s>>>(a, p);
-    cudaError_t e = cudaGetLastError();
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dense_kernel<F>, kThreads, 0);
     if (e != cudaSuccess) return e;
-    prefix_kernel<<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks);
+    const uint64_t wave = (uint64_t)(sms > 0 ? sms : 1) * (uint64_t)(per_sm > 0 ? per_sm : 1);
+    dense_kernel<F><<<(uint32_t)(tiles < wave ? tiles : wave), kThreads, 0, s>>>(a, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prefix_kernel<<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks, F::kSegs);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     place_kernel<F><<<(tiles + kWarps - 1) / kWarps, kThreads, 0, s>>>(a, p, tiles);
@@ -534,8 +543,6 @@ MultiLayout multi_layout(uint64_t n) {
     size_t off = kWsHeaderBytes;
     L.states = off;
     off += align256(8 * tiles);
-    L.tile_total = off;
-    off += align256(4 * tiles);
     L.tile_excl = off;
     off += align256(4 * tiles);
     L.seg_cnt = off;

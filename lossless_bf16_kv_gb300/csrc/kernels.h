@@ -62,13 +62,13 @@ struct CalibArgs {
 //   states               8 bytes per tile: look-back state words (the single-
 //                        launch pipeline uses one per tile, the tile-prefix
 //                        kernel one per 2048 tiles)
-//   tile_total, tile_excl  4 bytes per tile: escapes per tile and their
-//                        exclusive prefix
+//   tile_excl            4 bytes per tile: exclusive prefix of the tiles'
+//                        escape counts
 //   seg_cnt              32 x uint16 per tile: escapes per segment
 //   seg_ent              256 x uint16 per tile: the segments' first escapes
 //                        (position in segment | exponent << offset bits)
 struct MultiLayout {
-    size_t states, tile_total, tile_excl, seg_cnt, seg_ent, bytes;
+    size_t states, tile_excl, seg_cnt, seg_ent, bytes;
 };
 MultiLayout multi_layout(uint64_t n);
 
