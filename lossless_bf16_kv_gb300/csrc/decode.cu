@@ -6,17 +6,20 @@
 // reassemble sign, exponent and mantissa, and put the raw exponent of every
 // escape back at its position; the result is bitwise identical to the input.
 //
-// One launch, no communication between CTAs.  Each CTA decodes a fixed tile of
-// elements (8192 BF16, 16384 E5M2):
-//   1. it issues the loads of its dense streams (codes, sign+mantissa) first;
-//   2. while they are in flight it finds the tile's slice [lo, hi) of the
-//      escape stream (chunk_off at a chunk start, else a warp-wide search of
-//      the ascending positions inside the chunk), clears a per-element escape
-//      bitmap in shared memory and scatters the slice's raw exponents into a
-//      shared-memory byte array;
-//   3. each thread decodes its groups in registers: codebook lookup by byte
-//      permutes (the 16 entries live in four registers), SWAR reassembly,
-//      exponent patch where the bitmap says so, 16-byte stores.
+// One launch, no communication between CTAs and no barrier.  Warps walk
+// contiguous segments (1024 BF16 or 2048 E5M2 elements) grid-stride, one
+// segment ahead in a software pipeline:
+//   - the dense streams (codes, sign+mantissa) of the next segment and its
+//     slice [lo, hi) of the escape stream (chunk_off at a chunk start, else a
+//     warp-wide search of the ascending positions inside the chunk) are
+//     requested before the current segment is decoded, and its first 32
+//     escapes right after, so every round trip overlaps a segment's work;
+//   - each lane decodes its exponents in registers: codebook lookup by byte
+//     permutes (the 16 entries live in four registers);
+//   - the warp broadcasts each escape with shuffles; the lane that holds the
+//     element overwrites its exponent (escapes beyond the first 32 of a
+//     segment are read in further batches);
+//   - SWAR reassembly and 16-byte stores.
 // All escape metadata is clamped, so malformed streams cannot make the kernel
 // read or write out of bounds.
 #include <cstdint>
@@ -39,11 +42,6 @@ __device__ __forceinline__ uint32_t cb_lookup4(const uint32_t (&cb)[4], uint32_t
     const uint32_t t = c16 & 0x8888u;
     const uint32_t m = prmt(0x00008000u, 0u, t | (t >> 3));  // nibble 9 -> 0xFF, 0 -> 0x00
     return (hi & m) | (lo & ~m);
-}
-
-// 4-bit mask -> byte mask (bit k set -> byte k = 0xFF).
-__device__ __forceinline__ uint32_t expand_nibble(uint32_t b) {
-    return ((b * 0x00204081u) & 0x01010101u) * 0xFFu;
 }
 
 // Four BF16 values from four sign+mantissa bytes and four exponent bytes.
@@ -96,203 +94,310 @@ __device__ uint32_t escape_bound(const DecodeArgs& a, uint32_t x) {
     return lower_bound_warp(a.esc_pos, b, e, r);
 }
 
-// Steps 2 of the kernel: slice bounds, bitmap clear, scatter.  `exps` holds
-// kTile bytes, `mask` kTile/32 words.
-template <int kTile>
-__device__ __forceinline__ void scatter_escapes(const DecodeArgs& a, uint32_t t0,
-                                                uint8_t* exps, uint32_t* mask,
-                                                uint32_t* s_bounds) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t t1 = (uint64_t)t0 + kTile < a.n ? t0 + kTile : a.n;
-    if (warp == 0) {
-        const uint32_t lo = escape_bound(a, t0);
-        if (lane == 0) s_bounds[0] = lo;
-    } else if (warp == 1) {
-        const uint32_t hi = escape_bound(a, t1);
-        if (lane == 0) s_bounds[1] = hi;
+// Chunk of escape entry j: the largest c in [ca, cb] with chunk_off[c] <= j
+// (entries of empty chunks share offsets; the largest such c owns j).
+__device__ __forceinline__ uint32_t chunk_of_entry(const DecodeArgs& a, uint32_t j, uint32_t ca,
+                                                   uint32_t cb) {
+    uint32_t lo = ca, hi = cb;
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi + 1) >> 1;
+        if (clamp_off(a, mid) <= j) lo = mid;
+        else hi = mid - 1;
     }
-    for (int w = tid; w < kTile / 32; w += kThreads) mask[w] = 0;
-    __syncthreads();
-    const uint32_t lo = s_bounds[0], hi = max(s_bounds[0], s_bounds[1]);
-    if (lo == hi) return;
-    const uint32_t ca = t0 / a.cdiv.d, cb = (t1 - 1) / a.cdiv.d;
-    const uint32_t nc = cb - ca + 1;
-    auto scatter_chunk = [&](uint32_t c, uint32_t first, uint32_t step) {
-        const uint32_t b = max(clamp_off(a, c), lo);
-        const uint32_t e = min(clamp_off(a, c + 1), hi);
-        const uint32_t cbase = c * a.cdiv.d;
-        for (uint32_t j = b + first; j < e; j += step) {
-            const uint32_t p = a.esc_pos[j];
-            const uint32_t l = cbase + p - t0;  // wraps to a large value if below t0
-            if (p < a.cdiv.d && l < (uint32_t)kTile && cbase + p < t1) {
-                exps[l] = a.esc_val[j];
-                atomicOr(&mask[l >> 5], 1u << (l & 31));
+    return lo;
+}
+
+// A batch of up to 32 escapes of one segment, one per lane: entry j, its
+// position in chunk and raw exponent (j = 0xFFFFFFFF: no entry).
+struct EscBatch {
+    uint32_t j, pos, val;
+};
+
+__device__ __forceinline__ EscBatch load_batch(const DecodeArgs& a, uint32_t b, uint32_t hi) {
+    const uint32_t j = b + (threadIdx.x & 31);
+    EscBatch e{0xFFFFFFFFu, 0u, 0u};
+    if (j < hi) {
+        e.j = j;
+        e.pos = a.esc_pos[j];
+        e.val = a.esc_val[j];
+    }
+    return e;
+}
+
+// Broadcasts the batch's escapes of segment [s0, s1) and calls patch(local
+// index, raw exponent) on all lanes for each (warp-uniform).  Escapes whose
+// metadata points outside the segment are skipped.
+template <class Patch>
+__device__ __forceinline__ void apply_batch(const DecodeArgs& a, const EscBatch& e, uint32_t s0,
+                                            uint32_t s1, uint32_t ca, uint32_t cb, Patch& patch) {
+    uint32_t local = 0xFFFFFFFFu;
+    if (e.j != 0xFFFFFFFFu) {
+        const uint32_t c = ca == cb ? ca : chunk_of_entry(a, e.j, ca, cb);
+        const uint32_t x = c * a.cdiv.d + e.pos;
+        if (e.pos < a.cdiv.d && x >= s0 && x < s1) local = x - s0;
+    }
+    uint32_t m = __ballot_sync(0xFFFFFFFFu, local != 0xFFFFFFFFu);
+    while (m) {
+        const uint32_t src = __ffs(m) - 1;
+        m &= m - 1;
+        patch(__shfl_sync(0xFFFFFFFFu, local, src), __shfl_sync(0xFFFFFFFFu, e.val, src));
+    }
+}
+
+__device__ __forceinline__ uint32_t set_byte(uint32_t w, uint32_t byte, uint32_t v) {
+    const uint32_t sh = 8 * byte;
+    return (w & ~(0xFFu << sh)) | ((v & 0xFFu) << sh);
+}
+
+// Pipelined segment loop shared by both formats.  F provides:
+//   kSeg                        elements per warp segment
+//   struct Dense                the lane's dense stream words of a segment
+//   load(a, s0, s1, lane)       -> Dense
+//   decode(a, cb, d, ex)        exponents of the lane's elements
+//   patch(ex, local, val, lane) overwrite one exponent if the lane holds it
+//   store(a, s0, s1, lane, d, ex)
+template <class F>
+__device__ __forceinline__ void decode_segments(const DecodeArgs& a) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t warps = gridDim.x * kWarps;
+    const uint32_t nseg = (a.n + F::kSeg - 1) / F::kSeg;
+    const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
+    uint32_t seg = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (seg >= nseg) return;  // warp-uniform
+
+    auto bounds = [&](uint32_t sg, uint32_t& lo, uint32_t& hi) {
+        const uint32_t s0 = sg * (uint32_t)F::kSeg;
+        const uint32_t s1 = a.n - s0 < (uint32_t)F::kSeg ? a.n : s0 + F::kSeg;
+        lo = escape_bound(a, s0);
+        hi = max(lo, escape_bound(a, s1));
+    };
+    uint32_t lo, hi;
+    bounds(seg, lo, hi);
+    typename F::Dense d = F::load(a, seg * (uint32_t)F::kSeg, lane);
+    EscBatch eb = load_batch(a, lo, hi);
+    while (true) {
+        const uint32_t s0 = seg * (uint32_t)F::kSeg;
+        const uint32_t s1 = a.n - s0 < (uint32_t)F::kSeg ? a.n : s0 + F::kSeg;
+        const uint32_t next = seg + warps;
+        const bool more = next < nseg;
+        // Next segment's requests go out before this one is decoded.
+        typename F::Dense dn;
+        uint32_t lo_n = 0, hi_n = 0;
+        if (more) {
+            dn = F::load(a, next * (uint32_t)F::kSeg, lane);
+            bounds(next, lo_n, hi_n);
+        }
+        typename F::Ex ex;
+        F::decode(cb, d, ex);
+        if (lo < hi) {
+            const uint32_t ca = s0 / a.cdiv.d, cbk = (s1 - 1) / a.cdiv.d;
+            auto patch = [&](uint32_t local, uint32_t val) { F::patch(ex, local, val, lane); };
+            apply_batch(a, eb, s0, s1, ca, cbk, patch);
+            for (uint32_t b = lo + 32; b < hi; b += 32) {
+                const EscBatch more_eb = load_batch(a, b, hi);
+                apply_batch(a, more_eb, s0, s1, ca, cbk, patch);
             }
         }
-    };
-    if (nc >= (uint32_t)kWarps) {
-        for (uint32_t c = ca + warp; c <= cb; c += kWarps) scatter_chunk(c, lane, 32);
-    } else {
-        for (uint32_t c = ca; c <= cb; c++) scatter_chunk(c, tid, kThreads);
+        if (more) eb = load_batch(a, lo_n, hi_n);
+        F::store(a, s0, s1, lane, d, ex);
+        if (!more) break;
+        seg = next;
+        lo = lo_n;
+        hi = hi_n;
+        d = dn;
     }
 }
 
 // ------------------------------------------------------------------- BF16
-
-constexpr int kBf16Groups = 4;                          // groups of 8 per thread
-constexpr int kBf16Tile = kThreads * kBf16Groups * 8;  // 8192 elements
-constexpr uint32_t kBf16Stride = kThreads * 8;
-
-__global__ void __launch_bounds__(kThreads) decode_bf16_kernel(const DecodeArgs a) {
-    __shared__ __align__(16) uint8_t exps[kBf16Tile];
-    __shared__ uint32_t mask[kBf16Tile / 32];
-    __shared__ uint32_t s_bounds[2];
-
-    const int tid = threadIdx.x;
-    const uint32_t t0 = blockIdx.x * (uint32_t)kBf16Tile;
-    const bool full = (uint64_t)t0 + kBf16Tile <= a.n;
-    const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
-
-    uint32_t code[kBf16Groups];
-    uint2 sm[kBf16Groups];
+//
+// Segment [s0, s0 + 1024); lane l holds the groups of 8 at s0 + 256 k + 8 l
+// (k < 4): each warp load covers 128 code bytes and 256 sign+mantissa bytes,
+// each store 512 output bytes.
+struct Bf16Seg {
+    static constexpr int kSeg = 1024;
+    static constexpr int kGroups = 4;
+    struct Dense {
+        uint32_t code[kGroups];
+        uint2 sm[kGroups];
+    };
+    struct Ex {
+        uint32_t e[kGroups][2];
+    };
+    static __device__ __forceinline__ Dense load(const DecodeArgs& a, uint32_t s0, uint32_t lane) {
+        Dense d;
+        const uint32_t s1 = a.n - s0 < (uint32_t)kSeg ? a.n : s0 + kSeg;
+        const bool full = s1 - s0 == (uint32_t)kSeg;
 #pragma unroll
-    for (int k = 0; k < kBf16Groups; k++) {
-        const uint32_t i = t0 + k * kBf16Stride + tid * 8;
-        if (full || i + 8 <= a.n) {
-            code[k] = ld_stream4(a.codes + i / 2);
-            sm[k] = ld_stream8(a.signman + i);
-        } else {
-            code[k] = 0;
-            sm[k] = make_uint2(0, 0);
-            if (i < a.n) {
-                const uint32_t rem = a.n - i;
-                for (uint32_t j = 0; j < (rem + 1) / 2; j++)
-                    code[k] |= (uint32_t)a.codes[i / 2 + j] << (8 * j);
-                for (uint32_t j = 0; j < rem; j++) {
-                    const uint32_t b = (uint32_t)a.signman[i + j] << (8 * (j & 3));
-                    if (j < 4) sm[k].x |= b; else sm[k].y |= b;
+        for (int k = 0; k < kGroups; k++) {
+            const uint32_t i = s0 + 256 * k + 8 * lane;
+            if (full || i + 8 <= s1) {
+                d.code[k] = ld_stream4(a.codes + i / 2);
+                d.sm[k] = ld_stream8(a.signman + i);
+            } else {
+                d.code[k] = 0;
+                d.sm[k] = make_uint2(0, 0);
+                if (i < s1) {
+                    const uint32_t rem = s1 - i;
+                    for (uint32_t j = 0; j < (rem + 1) / 2; j++)
+                        d.code[k] |= (uint32_t)a.codes[i / 2 + j] << (8 * j);
+                    for (uint32_t j = 0; j < rem; j++) {
+                        const uint32_t b = (uint32_t)a.signman[i + j] << (8 * (j & 3));
+                        if (j < 4) d.sm[k].x |= b; else d.sm[k].y |= b;
+                    }
                 }
             }
         }
+        return d;
     }
-
-    scatter_escapes<kBf16Tile>(a, t0, exps, mask, s_bounds);
-    __syncthreads();
-
+    static __device__ __forceinline__ void decode(const uint32_t (&cb)[4], const Dense& d, Ex& ex) {
 #pragma unroll
-    for (int k = 0; k < kBf16Groups; k++) {
-        const uint32_t loff = k * kBf16Stride + tid * 8;
-        const uint32_t i = t0 + loff;
-        if (!full && i >= a.n) continue;
-        uint32_t ex0 = cb_lookup4(cb, code[k] & 0xFFFFu);
-        uint32_t ex1 = cb_lookup4(cb, code[k] >> 16);
-        const uint32_t mb = reinterpret_cast<const uint8_t*>(mask)[loff >> 3];
-        if (mb) {
-            const uint2 xv = *reinterpret_cast<const uint2*>(exps + loff);
-            const uint32_t m0 = expand_nibble(mb & 0xFu), m1 = expand_nibble(mb >> 4);
-            ex0 = (xv.x & m0) | (ex0 & ~m0);
-            ex1 = (xv.y & m1) | (ex1 & ~m1);
-        }
-        const uint2 o0 = assemble_bf16(sm[k].x, ex0);
-        const uint2 o1 = assemble_bf16(sm[k].y, ex1);
-        if (full || i + 8 <= a.n) {
-            st_stream16(a.y + 2ull * i, make_uint4(o0.x, o0.y, o1.x, o1.y));
-        } else {
-            const uint32_t w[4] = {o0.x, o0.y, o1.x, o1.y};
-            uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + i;
-            for (uint32_t j = 0; j < a.n - i; j++) yp[j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+        for (int k = 0; k < kGroups; k++) {
+            ex.e[k][0] = cb_lookup4(cb, d.code[k] & 0xFFFFu);
+            ex.e[k][1] = cb_lookup4(cb, d.code[k] >> 16);
         }
     }
-}
+    static __device__ __forceinline__ void patch(Ex& ex, uint32_t local, uint32_t val, uint32_t lane) {
+        if (((local >> 3) & 31u) != lane) return;
+        const uint32_t k = local >> 8, h = (local >> 2) & 1u, byte = local & 3u;
+#pragma unroll
+        for (int kk = 0; kk < kGroups; kk++)
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++)
+                if (kk == (int)k && hh == (int)h) ex.e[kk][hh] = set_byte(ex.e[kk][hh], byte, val);
+    }
+    static __device__ __forceinline__ void store(const DecodeArgs& a, uint32_t s0, uint32_t s1,
+                                                 uint32_t lane, const Dense& d, const Ex& ex) {
+        const bool full = s1 - s0 == (uint32_t)kSeg;
+#pragma unroll
+        for (int k = 0; k < kGroups; k++) {
+            const uint32_t i = s0 + 256 * k + 8 * lane;
+            if (!full && i >= s1) continue;
+            const uint2 o0 = assemble_bf16(d.sm[k].x, ex.e[k][0]);
+            const uint2 o1 = assemble_bf16(d.sm[k].y, ex.e[k][1]);
+            if (full || i + 8 <= s1) {
+                st_stream16(a.y + 2ull * i, make_uint4(o0.x, o0.y, o1.x, o1.y));
+            } else {
+                const uint32_t w[4] = {o0.x, o0.y, o1.x, o1.y};
+                uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + i;
+                for (uint32_t j = 0; j < s1 - i; j++) yp[j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+            }
+        }
+    }
+};
 
 // ------------------------------------------------------------------- E5M2
-
-constexpr int kE5m2Groups = 2;                          // groups of 32 per thread
-constexpr int kE5m2Tile = kThreads * kE5m2Groups * 32; // 16384 elements
-constexpr uint32_t kE5m2Stride = kThreads * 32;
-
-__global__ void __launch_bounds__(kThreads) decode_e5m2_kernel(const DecodeArgs a) {
-    __shared__ __align__(16) uint8_t exps[kE5m2Tile];
-    __shared__ uint32_t mask[kE5m2Tile / 32];
-    __shared__ uint32_t s_bounds[2];
-
-    const int tid = threadIdx.x;
-    const uint32_t t0 = blockIdx.x * (uint32_t)kE5m2Tile;
-    const bool full = (uint64_t)t0 + kE5m2Tile <= a.n;
-    const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
-
-    uint4 code[kE5m2Groups];
-    uint32_t smw[kE5m2Groups][3];
+//
+// Segment [s0, s0 + 2048); lane l holds the groups of 32 at s0 + 1024 k + 32 l
+// (k < 2): 16 code bytes and 12 bytes of packed 3-bit fields in, 32 output
+// bytes out per group.
+struct E5m2Seg {
+    static constexpr int kSeg = 2048;
+    static constexpr int kGroups = 2;
+    struct Dense {
+        uint4 code[kGroups];
+        uint32_t smw[kGroups][3];
+    };
+    struct Ex {
+        uint32_t e[kGroups][8];
+    };
+    static __device__ __forceinline__ Dense load(const DecodeArgs& a, uint32_t s0, uint32_t lane) {
+        Dense d;
+        const uint32_t s1 = a.n - s0 < (uint32_t)kSeg ? a.n : s0 + kSeg;
+        const bool full = s1 - s0 == (uint32_t)kSeg;
 #pragma unroll
-    for (int k = 0; k < kE5m2Groups; k++) {
-        const uint32_t i = t0 + k * kE5m2Stride + tid * 32;
-        const uint8_t* smp = a.signman + (uint64_t)(i / 32) * 12;
-        if (full || i + 32 <= a.n) {
-            code[k] = ld_stream16(a.codes + i / 2);
-            smw[k][0] = ld_stream4(smp);
-            smw[k][1] = ld_stream4(smp + 4);
-            smw[k][2] = ld_stream4(smp + 8);
-        } else {
-            uint32_t cw[4] = {0, 0, 0, 0};
-            smw[k][0] = smw[k][1] = smw[k][2] = 0;
-            if (i < a.n) {
-                const uint32_t rem = a.n - i;
-                for (uint32_t j = 0; j < (rem + 1) / 2; j++)
-                    cw[j >> 2] |= (uint32_t)a.codes[i / 2 + j] << (8 * (j & 3));
-                for (uint32_t j = 0; j < (3 * rem + 7) / 8; j++)
-                    smw[k][j >> 2] |= (uint32_t)smp[j] << (8 * (j & 3));
+        for (int k = 0; k < kGroups; k++) {
+            const uint32_t i = s0 + 1024 * k + 32 * lane;
+            const uint8_t* smp = a.signman + (uint64_t)(i / 32) * 12;
+            if (full || i + 32 <= s1) {
+                d.code[k] = ld_stream16(a.codes + i / 2);
+                d.smw[k][0] = ld_stream4(smp);
+                d.smw[k][1] = ld_stream4(smp + 4);
+                d.smw[k][2] = ld_stream4(smp + 8);
+            } else {
+                uint32_t cw[4] = {0, 0, 0, 0};
+                d.smw[k][0] = d.smw[k][1] = d.smw[k][2] = 0;
+                if (i < s1) {
+                    const uint32_t rem = s1 - i;
+                    for (uint32_t j = 0; j < (rem + 1) / 2; j++)
+                        cw[j >> 2] |= (uint32_t)a.codes[i / 2 + j] << (8 * (j & 3));
+                    for (uint32_t j = 0; j < (3 * rem + 7) / 8; j++)
+                        d.smw[k][j >> 2] |= (uint32_t)smp[j] << (8 * (j & 3));
+                }
+                d.code[k] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
             }
-            code[k] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        }
+        return d;
+    }
+    static __device__ __forceinline__ void decode(const uint32_t (&cb)[4], const Dense& d, Ex& ex) {
+#pragma unroll
+        for (int k = 0; k < kGroups; k++) {
+            const uint32_t cw[4] = {d.code[k].x, d.code[k].y, d.code[k].z, d.code[k].w};
+#pragma unroll
+            for (int m = 0; m < 8; m++)
+                ex.e[k][m] = cb_lookup4(cb, (cw[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
         }
     }
-
-    scatter_escapes<kE5m2Tile>(a, t0, exps, mask, s_bounds);
-    __syncthreads();
-
+    static __device__ __forceinline__ void patch(Ex& ex, uint32_t local, uint32_t val, uint32_t lane) {
+        if (((local >> 5) & 31u) != lane) return;
+        const uint32_t k = local >> 10, m = (local >> 2) & 7u, byte = local & 3u;
 #pragma unroll
-    for (int k = 0; k < kE5m2Groups; k++) {
-        const uint32_t loff = k * kE5m2Stride + tid * 32;
-        const uint32_t i = t0 + loff;
-        if (!full && i >= a.n) continue;
-        const uint32_t s0 = smw[k][0], s1 = smw[k][1], s2 = smw[k][2];
-        const uint32_t f12[8] = {
-            s0 & 0xFFFu, (s0 >> 12) & 0xFFFu, __funnelshift_r(s0, s1, 24) & 0xFFFu,
-            (s1 >> 4) & 0xFFFu, (s1 >> 16) & 0xFFFu, __funnelshift_r(s1, s2, 28) & 0xFFFu,
-            (s2 >> 8) & 0xFFFu, s2 >> 20};
-        const uint32_t cw[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
-        const uint32_t mword = mask[loff >> 5];
-        uint32_t out[8];
+        for (int kk = 0; kk < kGroups; kk++)
 #pragma unroll
-        for (int m = 0; m < 8; m++) {
-            uint32_t ex = cb_lookup4(cb, (cw[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
-            const uint32_t mb = (mword >> (4 * m)) & 0xFu;
-            if (mb) {
-                const uint32_t xv = *reinterpret_cast<const uint32_t*>(exps + loff + 4 * m);
-                const uint32_t mm = expand_nibble(mb);
-                ex = (xv & mm) | (ex & ~mm);
+            for (int mm = 0; mm < 8; mm++)
+                if (kk == (int)k && mm == (int)m) ex.e[kk][mm] = set_byte(ex.e[kk][mm], byte, val);
+    }
+    static __device__ __forceinline__ void store(const DecodeArgs& a, uint32_t s0, uint32_t s1,
+                                                 uint32_t lane, const Dense& d, const Ex& ex) {
+        const bool full = s1 - s0 == (uint32_t)kSeg;
+#pragma unroll
+        for (int k = 0; k < kGroups; k++) {
+            const uint32_t i = s0 + 1024 * k + 32 * lane;
+            if (!full && i >= s1) continue;
+            const uint32_t w0 = d.smw[k][0], w1 = d.smw[k][1], w2 = d.smw[k][2];
+            const uint32_t f12[8] = {
+                w0 & 0xFFFu, (w0 >> 12) & 0xFFFu, __funnelshift_r(w0, w1, 24) & 0xFFFu,
+                (w1 >> 4) & 0xFFFu, (w1 >> 16) & 0xFFFu, __funnelshift_r(w1, w2, 28) & 0xFFFu,
+                (w2 >> 8) & 0xFFFu, w2 >> 20};
+            uint32_t out[8];
+#pragma unroll
+            for (int m = 0; m < 8; m++) out[m] = assemble_e5m2(f12[m], ex.e[k][m]);
+            if (full || i + 32 <= s1) {
+                st_stream16(a.y + i, make_uint4(out[0], out[1], out[2], out[3]));
+                st_stream16(a.y + i + 16, make_uint4(out[4], out[5], out[6], out[7]));
+            } else {
+                for (uint32_t j = 0; j < s1 - i; j++) a.y[i + j] = (uint8_t)(out[j >> 2] >> (8 * (j & 3)));
             }
-            out[m] = assemble_e5m2(f12[m], ex);
-        }
-        if (full || i + 32 <= a.n) {
-            st_stream16(a.y + i, make_uint4(out[0], out[1], out[2], out[3]));
-            st_stream16(a.y + i + 16, make_uint4(out[4], out[5], out[6], out[7]));
-        } else {
-            for (uint32_t j = 0; j < a.n - i; j++) a.y[i + j] = (uint8_t)(out[j >> 2] >> (8 * (j & 3)));
         }
     }
+};
+
+template <class F>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
+    decode_segments<F>(a);
+}
+
+template <class F>
+cudaError_t launch_segments(const DecodeArgs& a, cudaStream_t s) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<F>, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    const uint64_t nseg = ((uint64_t)a.n + F::kSeg - 1) / F::kSeg;
+    const uint64_t ctas = (nseg + kWarps - 1) / kWarps;
+    const uint64_t wave = (uint64_t)(sms > 0 ? sms : 1) * (uint64_t)(per_sm > 0 ? per_sm : 1);
+    decode_kernel<F><<<(uint32_t)(ctas < wave ? ctas : wave), kThreads, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_tile_elems(bool e5m2) { return e5m2 ? kE5m2Tile : kBf16Tile; }
+int decode_tile_elems(bool e5m2) { return (e5m2 ? E5m2Seg::kSeg : Bf16Seg::kSeg) * kWarps; }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool e5m2, cudaStream_t s) {
-    if (a.num_tiles == 0) return cudaSuccess;
-    if (e5m2)
-        decode_e5m2_kernel<<<a.num_tiles, kThreads, 0, s>>>(a);
-    else
-        decode_bf16_kernel<<<a.num_tiles, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    if (a.n == 0) return cudaSuccess;
+    return e5m2 ? launch_segments<E5m2Seg>(a, s) : launch_segments<Bf16Seg>(a, s);
 }
 
 }  // namespace splitzip
