@@ -36,8 +36,12 @@ if ROOT not in sys.path:
 METRIC = "encode / decode GB/s (uncompressed bytes) and % of HBM roofline; compression ratio"
 DEFAULT_WORKLOAD = "kv_prefill_64L_16k"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS = {"encode": ("encode_bf16_kernel", "encode_e5m2_kernel"),
-           "decode": ("decode_bf16_kernel", "decode_e5m2_kernel")}
+# The encode call is three launches (dense pass, tile-prefix scan, escape
+# placement; the dense pass takes about 95% of the time), decode one.  The
+# roofline is taken per call: algorithmic bytes of the call over its time.
+KERNELS = {"encode": ("encode[dense_kernel+prefix_kernel+place_kernel]<Bf16Dense>",
+                      "encode[dense_kernel+prefix_kernel+place_kernel]<E5m2Dense>"),
+           "decode": ("decode_kernel<Bf16Seg>", "decode_kernel<E5m2Seg>")}
 
 
 # ------------------------------------------------------------ host helpers
@@ -54,6 +58,20 @@ def aggregate(times_s, units_per_rank: float):
     units_per_rank in its own time; the job took the slowest rank's time."""
     t = max(times_s)
     return units_per_rank * len(times_s) / t, t
+
+
+def max_over_ranks(seconds: float, device) -> list:
+    """The job's time as every rank sees it: one all_reduce(MAX) of each
+    rank's own timed region, repeated once per rank (so that aggregate() sees
+    world_size entries).  Without an initialised process group it is the
+    caller's own time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [seconds]
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [t.item()] * dist.get_world_size()
 
 
 def measured_peak_hbm():
@@ -249,11 +267,7 @@ def run_gpu(args):
     total_s = t_start.elapsed_time(t_end) / 1e3
     enc_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    times = [total_s]
-    if world > 1:
-        tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        times = [tt.item()] * world
+    times = max_over_ranks(total_s, dev)
     bytes_per_step = n * elem
     value_Bps, max_s = aggregate(times, bytes_per_step * K)
     res = {
@@ -432,7 +446,7 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--cpu-sample-elems", type=int, default=1 << 26)
+    ap.add_argument("--cpu-sample-elems", type=int, default=1 << 30)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, _ = dist_env()
@@ -476,7 +490,12 @@ def main():
                      if src == "measured" else "fallback", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": stored_traffic(kernel, w.name),
                      "algorithmic_bytes_per_launch": algo},
-        "gpu_launches": 2 * K,
+        "roofline_other": {"op": "decode" if dominant == "encode" else "encode",
+                           "achieved": round(algo / (min(enc, dec) / 1e3) / 1e9, 1),
+                           "frac": round(algo / (min(enc, dec) / 1e3) / 1e9 / peak, 4),
+                           "kernel": KERNELS["decode" if dominant == "encode" else "encode"][
+                               0 if res["fmt"] == "bf16" else 1]},
+        "gpu_launches": 4 * K,  # encode: dense, prefix, place; decode: one
         "clocks": res["clocks"],
         "context": {"pages_h200_encode_gbs": 613.3, "pages_h200_decode_gbs": 2181.8,
                     "note": "H200, real Qwen3-32B KV; another machine and data"},
