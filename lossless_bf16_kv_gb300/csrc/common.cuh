@@ -112,18 +112,28 @@ __device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
 // x < 2^17 and 1 <= d <= 2^16 (Granlund & Montgomery, "Division by Invariant
 // Integers using Multiplication", 1994): with m*d = 2^33 + e, 0 <= e < d, the
 // error term x*e / (d * 2^33) stays below 1/d because x*e < 2^17 * 2^16.
+//
+// For any 32-bit x, q = floor(x / d) is the high 64 bits of x * M with
+// M = ceil(2^64 / d) (Lemire, Kaser and Kurz, "Faster Remainder by Direct
+// Computation", 2019: exact for every 32-bit numerator and divisor d >= 2).
 struct ChunkDiv {
-    uint32_t d;  // chunk size
-    uint32_t m;  // ceil(2^33 / d)
+    uint32_t d;    // chunk size
+    uint32_t m;    // ceil(2^33 / d)
+    uint64_t m64;  // ceil(2^64 / d)
 };
 __host__ __device__ __forceinline__ ChunkDiv make_chunk_div(uint32_t d) {
     ChunkDiv c;
     c.d = d;
     c.m = (uint32_t)(((1ull << 33) + d - 1) / d);
+    c.m64 = d > 1 ? ~0ull / d + 1 : 0;
     return c;
 }
 __device__ __forceinline__ uint32_t chunk_quot(ChunkDiv c, uint32_t x) {
     return (uint32_t)(((uint64_t)x * c.m) >> 33);
+}
+// floor(x / d) for any 32-bit x (d >= 2).
+__device__ __forceinline__ uint32_t chunk_quot32(ChunkDiv c, uint32_t x) {
+    return (uint32_t)__umul64hi(c.m64, (uint64_t)x);
 }
 
 }  // namespace splitzip
@@ -184,6 +194,24 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
             "r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+// Per-thread asynchronous copies global -> shared (cp.async).  A thread that
+// waits for its own groups sees its own copies; no other thread's.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // Named barrier over the first `threads` threads of the CTA (id 1..15).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {

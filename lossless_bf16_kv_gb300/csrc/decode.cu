@@ -6,19 +6,22 @@
 // reassemble sign, exponent and mantissa, and put the raw exponent of every
 // escape back at its position; the result is bitwise identical to the input.
 //
-// One launch, no communication between CTAs and no barrier.  Warps walk
-// contiguous segments (1024 BF16 or 2048 E5M2 elements) grid-stride, one
-// segment ahead in a software pipeline:
-//   - the dense streams (codes, sign+mantissa) of the next segment and its
-//     slice [lo, hi) of the escape stream (chunk_off at a chunk start, else a
-//     warp-wide search of the ascending positions inside the chunk) are
-//     requested before the current segment is decoded, and its first 32
-//     escapes right after, so every round trip overlaps a segment's work;
+// One launch, no communication between CTAs and no CTA barrier.  Warps walk
+// contiguous segments (1024 BF16 or 2048 E5M2 elements) grid-stride:
+//   - the dense streams (codes, sign+mantissa) of a segment reach shared
+//     memory through a per-warp ring of kDecodeStages slots filled by cp.async
+//     (16 bytes per lane per copy, fully coalesced), kDecodeStages - 1
+//     segments ahead of the one being decoded;
+//   - the segment's slice [lo, hi) of the escape stream is found two segments
+//     ahead (chunk_off at a chunk start, else a warp-wide search of the
+//     ascending positions inside the chunk) and its first 32 escapes are
+//     loaded one segment ahead;
 //   - each lane decodes its exponents in registers: codebook lookup by byte
 //     permutes (the 16 entries live in four registers);
-//   - the warp broadcasts each escape with shuffles; the lane that holds the
-//     element overwrites its exponent (escapes beyond the first 32 of a
-//     segment are read in further batches);
+//   - a segment with escapes parks its exponent words in shared memory, each
+//     lane holding an escape overwrites that element's exponent byte, and the
+//     words are read back (escapes beyond the first 32 of a segment are read
+//     in further batches);
 //   - SWAR reassembly and 16-byte stores.
 // All escape metadata is clamped, so malformed streams cannot make the kernel
 // read or write out of bounds.
@@ -86,7 +89,7 @@ __device__ __forceinline__ uint32_t clamp_off(const DecodeArgs& a, uint32_t c) {
 // Index of the first escape of element x or later (x <= n).  All lanes call it.
 __device__ uint32_t escape_bound(const DecodeArgs& a, uint32_t x) {
     if (x >= a.n) return clamp_off(a, a.nchunks);
-    const uint32_t c = x / a.cdiv.d;
+    const uint32_t c = chunk_quot32(a.cdiv, x);
     const uint32_t r = x - c * a.cdiv.d;
     const uint32_t b = clamp_off(a, c);
     if (r == 0) return b;
@@ -124,47 +127,166 @@ __device__ __forceinline__ EscBatch load_batch(const DecodeArgs& a, uint32_t b, 
     return e;
 }
 
-// Broadcasts the batch's escapes of segment [s0, s1) and calls patch(local
-// index, raw exponent) on all lanes for each (warp-uniform).  Escapes whose
-// metadata points outside the segment are skipped.
-template <class Patch>
-__device__ __forceinline__ void apply_batch(const DecodeArgs& a, const EscBatch& e, uint32_t s0,
-                                            uint32_t s1, uint32_t ca, uint32_t cb, Patch& patch) {
-    uint32_t local = 0xFFFFFFFFu;
-    if (e.j != 0xFFFFFFFFu) {
-        const uint32_t c = ca == cb ? ca : chunk_of_entry(a, e.j, ca, cb);
-        const uint32_t x = c * a.cdiv.d + e.pos;
-        if (e.pos < a.cdiv.d && x >= s0 && x < s1) local = x - s0;
-    }
-    uint32_t m = __ballot_sync(0xFFFFFFFFu, local != 0xFFFFFFFFu);
-    while (m) {
-        const uint32_t src = __ffs(m) - 1;
-        m &= m - 1;
-        patch(__shfl_sync(0xFFFFFFFFu, local, src), __shfl_sync(0xFFFFFFFFu, e.val, src));
-    }
+// Element index (relative to the segment start s0) of batch entry e, or
+// 0xFFFFFFFF when the entry is absent or its metadata points outside the
+// segment [s0, s1); chunks ca..cb overlap the segment.
+__device__ __forceinline__ uint32_t batch_local(const DecodeArgs& a, const EscBatch& e,
+                                                uint32_t s0, uint32_t s1, uint32_t ca,
+                                                uint32_t cb) {
+    if (e.j == 0xFFFFFFFFu) return 0xFFFFFFFFu;
+    const uint32_t c = ca == cb ? ca : chunk_of_entry(a, e.j, ca, cb);
+    const uint32_t x = c * a.cdiv.d + e.pos;
+    return (e.pos < a.cdiv.d && x >= s0 && x < s1) ? x - s0 : 0xFFFFFFFFu;
 }
 
-__device__ __forceinline__ uint32_t set_byte(uint32_t w, uint32_t byte, uint32_t v) {
-    const uint32_t sh = 8 * byte;
-    return (w & ~(0xFFu << sh)) | ((v & 0xFFu) << sh);
+// Puts the raw exponents of escapes [lo, hi) of segment [s0, s1) into the
+// lane's exponent words: the words are parked in the warp's patch area, each
+// lane holding an escape (the first 32 in eb, then further batches) overwrites
+// its element's exponent byte, and the words are read back.  All lanes call it.
+template <class F>
+__device__ __forceinline__ void patch_escapes(const DecodeArgs& a, const EscBatch& eb, uint32_t lo,
+                                              uint32_t hi, uint32_t s0, uint32_t s1, uint32_t* pex,
+                                              typename F::Ex& ex) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t ca = chunk_quot32(a.cdiv, s0), cbk = chunk_quot32(a.cdiv, s1 - 1);
+#pragma unroll
+    for (int q = 0; q < F::kExWords; q++) pex[q * 32 + lane] = ex.e[q];
+    __syncwarp();
+    auto put = [&](const EscBatch& e) {
+        const uint32_t local = batch_local(a, e, s0, s1, ca, cbk);
+        if (local != 0xFFFFFFFFu) {
+            uint32_t q, l, byte;
+            F::locate(local, q, l, byte);
+            reinterpret_cast<uint8_t*>(pex)[(q * 32 + l) * 4 + byte] = (uint8_t)e.val;
+        }
+    };
+    put(eb);
+    for (uint32_t b = lo + 32; b < hi; b += 32) put(load_batch(a, b, hi));
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < F::kExWords; q++) ex.e[q] = pex[q * 32 + lane];
+    __syncwarp();  // the next segment's patch area writes come after these reads
 }
 
-// Pipelined segment loop shared by both formats.  F provides:
-//   kSeg                        elements per warp segment
-//   struct Dense                the lane's dense stream words of a segment
-//   load(a, s0, s1, lane)       -> Dense
-//   decode(a, cb, d, ex)        exponents of the lane's elements
-//   patch(ex, local, val, lane) overwrite one exponent if the lane holds it
+constexpr int kDecodeStages = 2;
+
+// Shared memory of a decode CTA: the patch area ([warp][exponent word][lane])
+// and, for a format decoded through the ring, the ring ([stage][warp][stage
+// bytes]) in front of it.
+template <class F>
+constexpr size_t decode_smem_bytes() {
+    return (F::kRing ? (size_t)kDecodeStages * kWarps * F::kStageBytes : 0) +
+           (size_t)kWarps * F::kExWords * 32 * 4;
+}
+
+// Segment loop shared by both formats.  F provides:
+//   kSeg, kStageBytes, kExWords   elements per segment, dense bytes per
+//                                 segment (codes first, then sign+mantissa),
+//                                 exponent words per lane
+//   sm_offset(s0)                 byte offset of the segment's sign+mantissa
+//   struct Dense / struct Ex      the lane's dense words / exponent words e[]
+//   read(stage, lane)             -> Dense, from a staged full segment
+//   load(a, s0, lane)             -> Dense, straight from global memory
+//   decode(cb, d, ex)             exponents of the lane's elements
+//   locate(local, q, l, byte)     exponent word q of lane l, byte, of element
+//                                 `local` of the segment
 //   store(a, s0, s1, lane, d, ex)
 template <class F>
-__device__ __forceinline__ void decode_segments(const DecodeArgs& a) {
-    const uint32_t lane = threadIdx.x & 31;
+__device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* smem) {
+    constexpr int S = kDecodeStages;
+    constexpr uint32_t kPieces = F::kStageBytes / 16;
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t warps = gridDim.x * kWarps;
+    const uint32_t nseg = (a.n + F::kSeg - 1) / F::kSeg;
+    const uint32_t full_segs = a.n / (uint32_t)F::kSeg;
+    const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
+    uint8_t* ring = smem + (size_t)warp * F::kStageBytes;  // stage s at ring + s * kWarps * kStageBytes
+    uint32_t* pex = reinterpret_cast<uint32_t*>(smem + (size_t)S * kWarps * F::kStageBytes) +
+                    (size_t)warp * F::kExWords * 32;
+    uint32_t seg = blockIdx.x * kWarps + warp;
+    if (seg >= nseg) return;  // warp-uniform
+
+    // Lanes copy the segment's dense bytes 16 at a time; a lane may read bytes
+    // another lane copied, so every read of a stage follows this lane's wait
+    // and a __syncwarp, and every refill follows a __syncwarp after the reads.
+    auto fill = [&](uint32_t sg, int stage) {
+        if (sg < full_segs) {
+            const uint32_t s0 = sg * (uint32_t)F::kSeg;
+            uint8_t* dst = ring + (size_t)stage * kWarps * F::kStageBytes;
+#pragma unroll
+            for (uint32_t q = 0; q < (kPieces + 31) / 32; q++) {
+                const uint32_t piece = q * 32 + lane;
+                if (piece < kPieces) {
+                    const uint32_t off = piece * 16;
+                    const uint8_t* src = off < (uint32_t)F::kCodeBytes
+                                             ? a.codes + s0 / 2 + off
+                                             : a.signman + F::sm_offset(s0) + (off - F::kCodeBytes);
+                    cp_async16(dst + off, src);
+                }
+            }
+        }
+        cp_async_commit();  // one group per segment, empty when not staged
+    };
+    auto bounds = [&](uint32_t sg, uint32_t& lo, uint32_t& hi) {
+        lo = hi = 0;
+        if (sg >= nseg) return;  // warp-uniform
+        const uint32_t s0 = sg * (uint32_t)F::kSeg;
+        const uint32_t s1 = a.n - s0 < (uint32_t)F::kSeg ? a.n : s0 + F::kSeg;
+        lo = escape_bound(a, s0);
+        hi = max(lo, escape_bound(a, s1));
+    };
+
+#pragma unroll
+    for (int st = 0; st < S; st++) fill(seg + st * warps, st);
+    uint32_t lo, hi, lo1, hi1;
+    bounds(seg, lo, hi);
+    bounds(seg + warps, lo1, hi1);
+    EscBatch eb = load_batch(a, lo, hi);
+    int stage = 0;
+    while (true) {
+        const uint32_t s0 = seg * (uint32_t)F::kSeg;
+        const uint32_t s1 = a.n - s0 < (uint32_t)F::kSeg ? a.n : s0 + F::kSeg;
+        const uint32_t next = seg + warps;
+        const bool more = next < nseg;
+        uint32_t lo2, hi2;
+        bounds(next + warps, lo2, hi2);  // two segments ahead
+        typename F::Dense d;
+        if (seg < full_segs) {
+            cp_async_wait<S - 1>();  // this segment's group (the oldest pending) has landed
+            __syncwarp();
+            d = F::read(ring + (size_t)stage * kWarps * F::kStageBytes, lane);
+        } else {
+            d = F::load(a, s0, lane);
+        }
+        typename F::Ex ex;
+        F::decode(cb, d, ex);
+        if (lo < hi) patch_escapes<F>(a, eb, lo, hi, s0, s1, pex, ex);  // warp-uniform
+        if (more) eb = load_batch(a, lo1, hi1);
+        F::store(a, s0, s1, lane, d, ex);
+        __syncwarp();  // every lane has read the stage before it is refilled
+        fill(seg + S * warps, stage);
+        stage = stage + 1 == S ? 0 : stage + 1;
+        if (!more) break;
+        seg = next;
+        lo = lo1;
+        hi = hi1;
+        lo1 = lo2;
+        hi1 = hi2;
+    }
+    cp_async_wait<0>();
+}
+
+// The same segment loop with the next segment's dense words prefetched into
+// registers instead of a shared-memory ring (one segment ahead).
+template <class F>
+__device__ __forceinline__ void decode_segments_regs(const DecodeArgs& a, uint8_t* smem) {
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t warps = gridDim.x * kWarps;
     const uint32_t nseg = (a.n + F::kSeg - 1) / F::kSeg;
     const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
-    uint32_t seg = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    uint32_t* pex = reinterpret_cast<uint32_t*>(smem) + (size_t)warp * F::kExWords * 32;
+    uint32_t seg = blockIdx.x * kWarps + warp;
     if (seg >= nseg) return;  // warp-uniform
-
     auto bounds = [&](uint32_t sg, uint32_t& lo, uint32_t& hi) {
         const uint32_t s0 = sg * (uint32_t)F::kSeg;
         const uint32_t s1 = a.n - s0 < (uint32_t)F::kSeg ? a.n : s0 + F::kSeg;
@@ -180,7 +302,6 @@ __device__ __forceinline__ void decode_segments(const DecodeArgs& a) {
         const uint32_t s1 = a.n - s0 < (uint32_t)F::kSeg ? a.n : s0 + F::kSeg;
         const uint32_t next = seg + warps;
         const bool more = next < nseg;
-        // Next segment's requests go out before this one is decoded.
         typename F::Dense dn;
         uint32_t lo_n = 0, hi_n = 0;
         if (more) {
@@ -189,15 +310,7 @@ __device__ __forceinline__ void decode_segments(const DecodeArgs& a) {
         }
         typename F::Ex ex;
         F::decode(cb, d, ex);
-        if (lo < hi) {
-            const uint32_t ca = s0 / a.cdiv.d, cbk = (s1 - 1) / a.cdiv.d;
-            auto patch = [&](uint32_t local, uint32_t val) { F::patch(ex, local, val, lane); };
-            apply_batch(a, eb, s0, s1, ca, cbk, patch);
-            for (uint32_t b = lo + 32; b < hi; b += 32) {
-                const EscBatch more_eb = load_batch(a, b, hi);
-                apply_batch(a, more_eb, s0, s1, ca, cbk, patch);
-            }
-        }
+        if (lo < hi) patch_escapes<F>(a, eb, lo, hi, s0, s1, pex, ex);  // warp-uniform
         if (more) eb = load_batch(a, lo_n, hi_n);
         F::store(a, s0, s1, lane, d, ex);
         if (!more) break;
@@ -211,18 +324,35 @@ __device__ __forceinline__ void decode_segments(const DecodeArgs& a) {
 // ------------------------------------------------------------------- BF16
 //
 // Segment [s0, s0 + 1024); lane l holds the groups of 8 at s0 + 256 k + 8 l
-// (k < 4): each warp load covers 128 code bytes and 256 sign+mantissa bytes,
-// each store 512 output bytes.
+// (k < 4): the warp's reads cover 128 code bytes and 256 sign+mantissa bytes
+// per group, each store 512 output bytes.  Stage layout: the segment's 512
+// code bytes, then its 1024 sign+mantissa bytes.
 struct Bf16Seg {
+    // Dense words prefetched into registers one segment ahead: at 2^31
+    // elements this measured 1.22 ms against 1.40 ms through the ring.
+    static constexpr bool kRing = false;
     static constexpr int kSeg = 1024;
     static constexpr int kGroups = 4;
+    static constexpr int kCodeBytes = kSeg / 2;
+    static constexpr int kStageBytes = kCodeBytes + kSeg;
+    static constexpr int kExWords = 2 * kGroups;
     struct Dense {
         uint32_t code[kGroups];
         uint2 sm[kGroups];
     };
     struct Ex {
-        uint32_t e[kGroups][2];
+        uint32_t e[kExWords];  // word 2k + h: elements 4h..4h+3 of group k
     };
+    static __device__ __forceinline__ uint32_t sm_offset(uint32_t s0) { return s0; }
+    static __device__ __forceinline__ Dense read(const uint8_t* stage, uint32_t lane) {
+        Dense d;
+#pragma unroll
+        for (int k = 0; k < kGroups; k++) {
+            d.code[k] = *reinterpret_cast<const uint32_t*>(stage + 128 * k + 4 * lane);
+            d.sm[k] = *reinterpret_cast<const uint2*>(stage + kCodeBytes + 256 * k + 8 * lane);
+        }
+        return d;
+    }
     static __device__ __forceinline__ Dense load(const DecodeArgs& a, uint32_t s0, uint32_t lane) {
         Dense d;
         const uint32_t s1 = a.n - s0 < (uint32_t)kSeg ? a.n : s0 + kSeg;
@@ -252,18 +382,15 @@ struct Bf16Seg {
     static __device__ __forceinline__ void decode(const uint32_t (&cb)[4], const Dense& d, Ex& ex) {
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
-            ex.e[k][0] = cb_lookup4(cb, d.code[k] & 0xFFFFu);
-            ex.e[k][1] = cb_lookup4(cb, d.code[k] >> 16);
+            ex.e[2 * k] = cb_lookup4(cb, d.code[k] & 0xFFFFu);
+            ex.e[2 * k + 1] = cb_lookup4(cb, d.code[k] >> 16);
         }
     }
-    static __device__ __forceinline__ void patch(Ex& ex, uint32_t local, uint32_t val, uint32_t lane) {
-        if (((local >> 3) & 31u) != lane) return;
-        const uint32_t k = local >> 8, h = (local >> 2) & 1u, byte = local & 3u;
-#pragma unroll
-        for (int kk = 0; kk < kGroups; kk++)
-#pragma unroll
-            for (int hh = 0; hh < 2; hh++)
-                if (kk == (int)k && hh == (int)h) ex.e[kk][hh] = set_byte(ex.e[kk][hh], byte, val);
+    static __device__ __forceinline__ void locate(uint32_t local, uint32_t& q, uint32_t& l,
+                                                  uint32_t& byte) {
+        q = 2 * (local >> 8) + ((local >> 2) & 1u);
+        l = (local >> 3) & 31u;
+        byte = local & 3u;
     }
     static __device__ __forceinline__ void store(const DecodeArgs& a, uint32_t s0, uint32_t s1,
                                                  uint32_t lane, const Dense& d, const Ex& ex) {
@@ -272,8 +399,8 @@ struct Bf16Seg {
         for (int k = 0; k < kGroups; k++) {
             const uint32_t i = s0 + 256 * k + 8 * lane;
             if (!full && i >= s1) continue;
-            const uint2 o0 = assemble_bf16(d.sm[k].x, ex.e[k][0]);
-            const uint2 o1 = assemble_bf16(d.sm[k].y, ex.e[k][1]);
+            const uint2 o0 = assemble_bf16(d.sm[k].x, ex.e[2 * k]);
+            const uint2 o1 = assemble_bf16(d.sm[k].y, ex.e[2 * k + 1]);
             if (full || i + 8 <= s1) {
                 st_stream16(a.y + 2ull * i, make_uint4(o0.x, o0.y, o1.x, o1.y));
             } else {
@@ -289,17 +416,38 @@ struct Bf16Seg {
 //
 // Segment [s0, s0 + 2048); lane l holds the groups of 32 at s0 + 1024 k + 32 l
 // (k < 2): 16 code bytes and 12 bytes of packed 3-bit fields in, 32 output
-// bytes out per group.
+// bytes out per group.  Stage layout: the segment's 1024 code bytes, then its
+// 768 bytes of 3-bit fields.
 struct E5m2Seg {
+    // Dense words through the two-stage ring: at 2^31 elements this measured
+    // 0.94 ms against 0.96 ms with register prefetch.
+    static constexpr bool kRing = true;
     static constexpr int kSeg = 2048;
     static constexpr int kGroups = 2;
+    static constexpr int kCodeBytes = kSeg / 2;
+    static constexpr int kStageBytes = kCodeBytes + kSeg * 3 / 8;
+    static constexpr int kExWords = 8 * kGroups;
     struct Dense {
         uint4 code[kGroups];
         uint32_t smw[kGroups][3];
     };
     struct Ex {
-        uint32_t e[kGroups][8];
+        uint32_t e[kExWords];  // word 8k + m: elements 4m..4m+3 of group k
     };
+    static __device__ __forceinline__ uint32_t sm_offset(uint32_t s0) { return s0 / 8 * 3; }
+    static __device__ __forceinline__ Dense read(const uint8_t* stage, uint32_t lane) {
+        Dense d;
+#pragma unroll
+        for (int k = 0; k < kGroups; k++) {
+            d.code[k] = *reinterpret_cast<const uint4*>(stage + 512 * k + 16 * lane);
+            const uint32_t* w =
+                reinterpret_cast<const uint32_t*>(stage + kCodeBytes + 384 * k + 12 * lane);
+            d.smw[k][0] = w[0];
+            d.smw[k][1] = w[1];
+            d.smw[k][2] = w[2];
+        }
+        return d;
+    }
     static __device__ __forceinline__ Dense load(const DecodeArgs& a, uint32_t s0, uint32_t lane) {
         Dense d;
         const uint32_t s1 = a.n - s0 < (uint32_t)kSeg ? a.n : s0 + kSeg;
@@ -334,17 +482,14 @@ struct E5m2Seg {
             const uint32_t cw[4] = {d.code[k].x, d.code[k].y, d.code[k].z, d.code[k].w};
 #pragma unroll
             for (int m = 0; m < 8; m++)
-                ex.e[k][m] = cb_lookup4(cb, (cw[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
+                ex.e[8 * k + m] = cb_lookup4(cb, (cw[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
         }
     }
-    static __device__ __forceinline__ void patch(Ex& ex, uint32_t local, uint32_t val, uint32_t lane) {
-        if (((local >> 5) & 31u) != lane) return;
-        const uint32_t k = local >> 10, m = (local >> 2) & 7u, byte = local & 3u;
-#pragma unroll
-        for (int kk = 0; kk < kGroups; kk++)
-#pragma unroll
-            for (int mm = 0; mm < 8; mm++)
-                if (kk == (int)k && mm == (int)m) ex.e[kk][mm] = set_byte(ex.e[kk][mm], byte, val);
+    static __device__ __forceinline__ void locate(uint32_t local, uint32_t& q, uint32_t& l,
+                                                  uint32_t& byte) {
+        q = 8 * (local >> 10) + ((local >> 2) & 7u);
+        l = (local >> 5) & 31u;
+        byte = local & 3u;
     }
     static __device__ __forceinline__ void store(const DecodeArgs& a, uint32_t s0, uint32_t s1,
                                                  uint32_t lane, const Dense& d, const Ex& ex) {
@@ -360,7 +505,7 @@ struct E5m2Seg {
                 (w2 >> 8) & 0xFFFu, w2 >> 20};
             uint32_t out[8];
 #pragma unroll
-            for (int m = 0; m < 8; m++) out[m] = assemble_e5m2(f12[m], ex.e[k][m]);
+            for (int m = 0; m < 8; m++) out[m] = assemble_e5m2(f12[m], ex.e[8 * k + m]);
             if (full || i + 32 <= s1) {
                 st_stream16(a.y + i, make_uint4(out[0], out[1], out[2], out[3]));
                 st_stream16(a.y + i + 16, make_uint4(out[4], out[5], out[6], out[7]));
@@ -373,21 +518,27 @@ struct E5m2Seg {
 
 template <class F>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
-    decode_segments<F>(a);
+    extern __shared__ __align__(16) uint8_t smem[];
+    if constexpr (F::kRing) decode_segments<F>(a, smem);
+    else decode_segments_regs<F>(a, smem);
 }
 
 template <class F>
 cudaError_t launch_segments(const DecodeArgs& a, cudaStream_t s) {
+    constexpr size_t smem = decode_smem_bytes<F>();
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<F>, kThreads, 0);
+        e = cudaFuncSetAttribute(decode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<F>, kThreads, smem);
     if (e != cudaSuccess) return e;
     const uint64_t nseg = ((uint64_t)a.n + F::kSeg - 1) / F::kSeg;
     const uint64_t ctas = (nseg + kWarps - 1) / kWarps;
     const uint64_t wave = (uint64_t)(sms > 0 ? sms : 1) * (uint64_t)(per_sm > 0 ? per_sm : 1);
-    decode_kernel<F><<<(uint32_t)(ctas < wave ? ctas : wave), kThreads, 0, s>>>(a);
+    decode_kernel<F><<<(uint32_t)(ctas < wave ? ctas : wave), kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

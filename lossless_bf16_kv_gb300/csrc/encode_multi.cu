@@ -9,11 +9,12 @@
 // The only cross-tile dependency of the format is the escape stream's order
 // (chunk, then position) and its offsets.  Here it is taken out of the
 // streaming pass:
-//   K1 dense     one CTA per 8192-element tile, no inter-CTA communication:
-//                16-byte loads, field split, table lookup, nibble packing,
+//   K1 dense     grid-stride over 8192-element tiles, no inter-CTA
+//                communication: input staged through a per-thread cp.async
+//                ring, field split, code lookup in shared-memory word tables,
 //                dense code and sign+mantissa stores.  Each warp ranks the
-//                escapes of its segments with shuffles and stores the count
-//                and the first few escapes of every segment in the
+//                escapes of its segments with one shuffle scan and stores the
+//                counts and the first few escapes of every segment in the
 //                workspace.
 //   K2 prefix    exclusive prefix of the per-tile escape counts (sums of the
 //                segment counts; 2048 tiles per CTA,
@@ -23,9 +24,9 @@
 //                A segment with more escapes than its workspace share is
 //                rebuilt from the input in element order.
 // Segments: BF16 -- the 256 consecutive elements warp w covers with its group
-// k (k-major: segment 8k + w), 8 workspace entries each; E5M2 -- the 1024
-// elements of warp w, 32 entries each.  Entries hold the position in the
-// segment and the raw exponent.
+// k (element order 8k + w, workspace slot 4w + k), 8 workspace entries each;
+// E5M2 -- the 1024 elements of warp w, 32 entries each.  Entries hold the
+// position in the segment and the raw exponent.
 #include <cstdint>
 
 #include "common.cuh"
@@ -54,38 +55,32 @@ __device__ __forceinline__ void build_table(uint8_t* table, const uint32_t (&cbw
     const int tid = threadIdx.x;
     table[tid] = (uint8_t)kMissEntry;
     __syncthreads();
-    if (tid < 16) table[(cbw[tid >> 2] >> (8 * (tid & 3))) & 0xFFu] = (uint8_t)tid;
+    // Static indices only: a dynamic index into the kernel parameters would
+    // make the compiler copy them to local memory.
+    const uint32_t q = (uint32_t)tid >> 2;
+    const uint32_t w = q == 0 ? cbw[0] : q == 1 ? cbw[1] : q == 2 ? cbw[2] : cbw[3];
+    if (tid < 16) table[(w >> (8 * (tid & 3))) & 0xFFu] = (uint8_t)tid;
     __syncthreads();
 }
 
-// Warp-wide exclusive scan of up to four small counts per lane (packed two
-// to a word): rel[k] = sum of c[k] over lower lanes, tot[k] = warp sum.
-template <int G>
-__device__ __forceinline__ void warp_scan(const uint32_t (&c)[G], uint32_t (&rel)[G],
-                                          uint32_t (&tot)[G]) {
-    const int lane = threadIdx.x & 31;
-    uint32_t p01 = c[0] | (G > 1 ? c[1] << 16 : 0u);
-    uint32_t p23 = (G > 2 ? c[2] : 0u) | (G > 3 ? c[3] << 16 : 0u);
-    const uint32_t own01 = p01, own23 = p23;
+// Warp-wide exclusive scan of one word per lane, excl = sum of p over the
+// lower lanes.  Also returns lane 31's exclusive prefix and word, from which
+// the caller forms the warp totals (the formats pack several small counts in
+// p, each field wide enough for its exclusive prefix but not necessarily for
+// the total).
+__device__ __forceinline__ void warp_scan_excl(uint32_t p, uint32_t& excl, uint32_t& e31,
+                                               uint32_t& p31) {
+    const uint32_t lane = threadIdx.x & 31;
+    uint32_t x = __shfl_up_sync(0xFFFFFFFFu, p, 1);
+    x = lane ? x : 0u;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, p01, d);
-        if (lane >= d) p01 += u;
-        if (G > 2) {
-            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, p23, d);
-            if (lane >= d) p23 += v;
-        }
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+        if (lane >= (uint32_t)d) x += y;
     }
-    const uint32_t t01 = __shfl_sync(0xFFFFFFFFu, p01, 31);
-    const uint32_t t23 = G > 2 ? __shfl_sync(0xFFFFFFFFu, p23, 31) : 0u;
-    const uint32_t e01 = p01 - own01, e23 = p23 - own23;
-    const uint32_t ex[4] = {e01 & 0xFFFFu, e01 >> 16, e23 & 0xFFFFu, e23 >> 16};
-    const uint32_t tt[4] = {t01 & 0xFFFFu, t01 >> 16, t23 & 0xFFFFu, t23 >> 16};
-#pragma unroll
-    for (int k = 0; k < G; k++) {
-        rel[k] = ex[k];
-        tot[k] = tt[k];
-    }
+    excl = x;
+    e31 = __shfl_sync(0xFFFFFFFFu, x, 31);
+    p31 = __shfl_sync(0xFFFFFFFFu, p, 31);
 }
 
 // ------------------------------------------------------------------- BF16
@@ -93,6 +88,16 @@ __device__ __forceinline__ void warp_scan(const uint32_t (&c)[G], uint32_t (&rel
 // Thread t's groups of 8 at tile offsets k*2048 + 8t (k < 4): each warp load
 // covers 512 contiguous input bytes and each warp store 128 code bytes and
 // 256 sign+mantissa bytes.
+//
+// The exponent -> code map is four 256-entry word tables in shared memory,
+// one per element position j within a half group of four:
+//   T_j[e] = code(e) << 4j          for e in the codebook,
+//   T_j[e] = 1 << (16 + j)          for an escape (code 0, flag bit).
+// The four entries of elements 4h..4h+3 occupy disjoint bits, so their sum is
+// the half group's four code nibbles (bits 0..15) and escape flags (bits
+// 16..19).  The sign+mantissa byte of a value is the sum of its masked low
+// byte (mantissa) and high byte (sign): (w & 0x807F807F) * 257 leaves both
+// values' bytes in bytes 1 and 3 of the product, with no carries.
 struct Bf16Dense {
     static constexpr int kGroups = 4;
     static constexpr int kSegs = 32;
@@ -100,48 +105,102 @@ struct Bf16Dense {
     static constexpr int kSegCap = kEntries / kSegs;  // 8
     static constexpr int kOffBits = 8;
     static constexpr uint32_t kExpMask = 0xFFu;
+    struct Tables {
+        uint32_t t[4][256];
+    };
     struct Keep {
-        uint32_t ex[kGroups][2], ent[kGroups][2], cnt[kGroups];
+        uint4 v[kGroups];       // the input words (escape exponents are re-read from them)
+        uint32_t miss[kGroups]; // escape flags: bits 0..3 elements 0..3, bits 16..19 elements 4..7
+        uint32_t cnt;           // escapes of group k in byte k (at most 8 each)
     };
     static __device__ __forceinline__ uint32_t loff(int k) {
         return k * (kThreads * 8) + threadIdx.x * 8;
     }
-    static __device__ __forceinline__ uint32_t seg(int k) { return k * kWarps + (threadIdx.x >> 5); }
+    // Segment 8k + w (element order: group k of warp w) is kept at workspace
+    // slot 4w + k, so that a warp's four counts are one 8-byte store.
+    static __device__ __forceinline__ uint32_t slot(int k) { return (threadIdx.x >> 5) * 4 + k; }
+    static __device__ __forceinline__ uint32_t storage(uint32_t s) { return (s & 7u) * 4 + (s >> 3); }
+    // Lane 0 stores the warp's four segment totals (16 bits each).
+    static __device__ __forceinline__ void store_counts(uint16_t* row, uint32_t e31, uint32_t p31) {
+        const uint32_t t02 = (e31 & 0x00FF00FFu) + (p31 & 0x00FF00FFu);
+        const uint32_t t13 = ((e31 >> 8) & 0x00FF00FFu) + ((p31 >> 8) & 0x00FF00FFu);
+        *reinterpret_cast<uint2*>(row + slot(0)) =
+            make_uint2(__byte_perm(t02, t13, 0x5410), __byte_perm(t02, t13, 0x7632));
+    }
 
-    static __device__ __forceinline__ void process(const EncodeArgs& a, const uint8_t* table,
-                                                   uint32_t t0, Keep& kp) {
-        const bool full = (uint64_t)t0 + kTileElems <= a.n;
-        if (full) {
-            uint4 v[kGroups];
+    static __device__ __forceinline__ void build_tables(Tables& tb, const uint32_t (&cbw)[4]) {
+        const uint32_t tid = threadIdx.x;
 #pragma unroll
-            for (int k = 0; k < kGroups; k++) v[k] = ld_stream16(a.x + 2ull * (t0 + loff(k)));
-            uint32_t sm[kGroups][2];
+        for (int j = 0; j < 4; j++) tb.t[j][tid] = 1u << (16 + j);
+        __syncthreads();
+        if (tid < 16) {
+            const uint32_t q = tid >> 2;
+            const uint32_t w = q == 0 ? cbw[0] : q == 1 ? cbw[1] : q == 2 ? cbw[2] : cbw[3];
+            const uint32_t e = (w >> (8 * (tid & 3))) & 0xFFu;
 #pragma unroll
-            for (int k = 0; k < kGroups; k++) {
-                split_bf16(v[k].x, v[k].y, sm[k][0], kp.ex[k][0]);
-                split_bf16(v[k].z, v[k].w, sm[k][1], kp.ex[k][1]);
-            }
-#pragma unroll
-            for (int k = 0; k < kGroups; k++) {
-                kp.ent[k][0] = lookup4(table, kp.ex[k][0]);
-                kp.ent[k][1] = lookup4(table, kp.ex[k][1]);
-            }
-#pragma unroll
-            for (int k = 0; k < kGroups; k++) {
-                const uint32_t i = t0 + loff(k);
-                kp.cnt[k] = miss_count(kp.ent[k][0], kp.ent[k][1]);
-                st_stream4(a.codes + i / 2, pack_nibbles(kp.ent[k][0], kp.ent[k][1]));
-                st_stream8(a.signman + i, make_uint2(sm[k][0], sm[k][1]));
-            }
-            return;
+            for (int j = 0; j < 4; j++) tb.t[j][e] = tid << (4 * j);
         }
-        const uint32_t pad = (a.cbw[0] & 0xFFu) << 7;  // exponent cb[0], sign 0, mantissa 0: code 0
-        const uint16_t* xs = reinterpret_cast<const uint16_t*>(a.x);
+        __syncthreads();
+    }
+
+    // Table entry of table j for the exponent at bits 7..14 (lo) or 23..30 (hi)
+    // of word w.
+    static __device__ __forceinline__ uint32_t ent_lo(const Tables& tb, int j, uint32_t w) {
+        return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(tb.t[j]) +
+                                                  ((w >> 5) & 0x3FCu));
+    }
+    static __device__ __forceinline__ uint32_t ent_hi(const Tables& tb, int j, uint32_t w) {
+        return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(tb.t[j]) +
+                                                  ((w >> 21) & 0x3FCu));
+    }
+    // Codes, sign+mantissa bytes and escape flags of the 8 values in v.
+    static __device__ __forceinline__ void group(const Tables& tb, const uint4& v, uint32_t& codes,
+                                                 uint2& sm, uint32_t& miss) {
+        const uint32_t u0 = (v.x & 0x807F807Fu) * 257u, u1 = (v.y & 0x807F807Fu) * 257u;
+        const uint32_t u2 = (v.z & 0x807F807Fu) * 257u, u3 = (v.w & 0x807F807Fu) * 257u;
+        sm = make_uint2(__byte_perm(u0, u1, 0x7531), __byte_perm(u2, u3, 0x7531));
+        const uint32_t A = ent_lo(tb, 0, v.x) + ent_hi(tb, 1, v.x) + ent_lo(tb, 2, v.y) + ent_hi(tb, 3, v.y);
+        const uint32_t B = ent_lo(tb, 0, v.z) + ent_hi(tb, 1, v.z) + ent_lo(tb, 2, v.w) + ent_hi(tb, 3, v.w);
+        codes = __byte_perm(A, B, 0x5410);
+        miss = __byte_perm(A, B, 0x7632);
+    }
+
+    // Input words of a full tile: load k of thread t is the 16 bytes of its
+    // group k, staged at ring slot [k][t].
+    static constexpr int kLoads = kGroups;
+    static __device__ __forceinline__ const uint8_t* load_src(const EncodeArgs& a, uint32_t t0,
+                                                             int k) {
+        return a.x + 2ull * (t0 + loff(k));
+    }
+    static __device__ __forceinline__ void compute_full(const EncodeArgs& a, const Tables& tb,
+                                                        uint32_t t0, const uint4 (&v)[kLoads],
+                                                        Keep& kp) {
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
             const uint32_t i = t0 + loff(k);
-            kp.cnt[k] = 0;
-            kp.ent[k][0] = kp.ent[k][1] = 0;
+            uint32_t codes, miss;
+            uint2 sm;
+            group(tb, v[k], codes, sm, miss);
+            kp.v[k] = v[k];
+            kp.miss[k] = miss;
+            st_stream4(a.codes + i / 2, codes);
+            st_stream8(a.signman + i, sm);
+        }
+        kp.cnt = __popc(kp.miss[0]) | (__popc(kp.miss[1]) << 8) | (__popc(kp.miss[2]) << 16) |
+                 (__popc(kp.miss[3]) << 24);
+    }
+
+    // The last, partial tile (element by element at its end).
+    static __device__ __forceinline__ void process_partial(const EncodeArgs& a, const Tables& tb,
+                                                           uint32_t t0, Keep& kp) {
+        const uint32_t pad = (a.cbw[0] & 0xFFu) << 7;  // exponent cb[0], sign 0, mantissa 0: code 0
+        const uint16_t* xs = reinterpret_cast<const uint16_t*>(a.x);
+        kp.cnt = 0;
+#pragma unroll
+        for (int k = 0; k < kGroups; k++) {
+            const uint32_t i = t0 + loff(k);
+            kp.miss[k] = 0;
+            kp.v[k] = make_uint4(0, 0, 0, 0);
             if (i >= a.n) continue;
             const uint32_t rem = a.n - i;
             const bool whole = rem >= 8;
@@ -156,40 +215,42 @@ struct Bf16Dense {
                            ((2u * m + 1 < rem ? (uint32_t)xs[i + 2 * m + 1] : pad) << 16);
                 v = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            uint32_t sm0, sm1;
-            split_bf16(v.x, v.y, sm0, kp.ex[k][0]);
-            split_bf16(v.z, v.w, sm1, kp.ex[k][1]);
-            kp.ent[k][0] = lookup4(table, kp.ex[k][0]);
-            kp.ent[k][1] = lookup4(table, kp.ex[k][1]);
-            const uint32_t codes = pack_nibbles(kp.ent[k][0], kp.ent[k][1]);
-            kp.cnt[k] = miss_count(kp.ent[k][0], kp.ent[k][1]);
+            uint32_t codes, miss;
+            uint2 sm;
+            group(tb, v, codes, sm, miss);
+            kp.v[k] = v;
+            kp.miss[k] = miss;
+            kp.cnt |= (uint32_t)__popc(miss) << (8 * k);
             if (whole) {
                 st_stream4(a.codes + i / 2, codes);
-                st_stream8(a.signman + i, make_uint2(sm0, sm1));
+                st_stream8(a.signman + i, sm);
             } else {
                 for (uint32_t j = 0; j < (rem + 1) / 2; j++) a.codes[i / 2 + j] = (uint8_t)(codes >> (8 * j));
                 for (uint32_t j = 0; j < rem; j++)
-                    a.signman[i + j] = (uint8_t)((j < 4 ? sm0 : sm1) >> (8 * (j & 3)));
+                    a.signman[i + j] = (uint8_t)((j < 4 ? sm.x : sm.y) >> (8 * (j & 3)));
             }
         }
     }
 
     // The first kSegCap escapes of each segment into its workspace entries.
-    static __device__ __forceinline__ void emit(const Keep& kp, const uint32_t (&rel)[kGroups],
-                                                uint16_t* ent) {
+    // excl: the exclusive escape ranks of this lane's groups, one per byte.
+    static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent) {
         const uint32_t lane = threadIdx.x & 31;
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
-            if (!kp.cnt[k]) continue;
-            uint32_t g = rel[k];
-            uint16_t* e = ent + seg(k) * kSegCap;
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                if ((kp.ent[k][j >> 2] >> (8 * (j & 3))) & kMissEntry) {
-                    if (g < (uint32_t)kSegCap)
-                        e[g] = (uint16_t)((8 * lane + j) | (((kp.ex[k][j >> 2] >> (8 * (j & 3))) & kExpMask) << kOffBits));
-                    g++;
-                }
+            uint32_t m = kp.miss[k];
+            if (!m) continue;
+            uint32_t g = (excl >> (8 * k)) & 0xFFu;
+            uint16_t* e = ent + slot(k) * kSegCap;
+            const uint32_t w[4] = {kp.v[k].x, kp.v[k].y, kp.v[k].z, kp.v[k].w};
+            while (m && g < (uint32_t)kSegCap) {
+                const uint32_t b = __ffs(m) - 1;  // bit b: element (b & 3) + 4 * (b >> 4)
+                m &= m - 1;
+                const uint32_t j = (b & 3u) + ((b >> 4) << 2);
+                const uint32_t word = j >> 1;
+                const uint32_t wv = word == 0 ? w[0] : word == 1 ? w[1] : word == 2 ? w[2] : w[3];
+                const uint32_t ex = (wv >> (7 + 16 * (j & 1))) & kExpMask;
+                e[g++] = (uint16_t)((8 * lane + j) | (ex << kOffBits));
             }
         }
     }
@@ -205,26 +266,47 @@ struct Bf16Dense {
 // Thread t's group is the 32 elements at tile offset 32t: 16 code bytes and
 // 12 bytes of packed 3-bit fields (three 4-byte stores).
 struct E5m2Dense {
-    static constexpr int kGroups = 1;
     static constexpr int kSegs = kWarps;              // 8
     static constexpr int kSegLen = 1024;
     static constexpr int kSegCap = kEntries / kSegs;  // 32
     static constexpr int kOffBits = 10;
     static constexpr uint32_t kExpMask = 0x1Fu;
-    struct Keep {
-        uint32_t ex[8], ent[8], cnt[kGroups];
+    struct Tables {
+        uint8_t t[256];
     };
-    static __device__ __forceinline__ uint32_t seg(int) { return threadIdx.x >> 5; }
+    struct Keep {
+        uint32_t ex[8], ent[8], cnt;
+    };
+    static __device__ __forceinline__ void build_tables(Tables& tb, const uint32_t (&cbw)[4]) {
+        build_table(tb.t, cbw);
+    }
+    static __device__ __forceinline__ uint32_t slot(int) { return threadIdx.x >> 5; }
+    static __device__ __forceinline__ uint32_t storage(uint32_t s) { return s; }
+    static __device__ __forceinline__ void store_counts(uint16_t* row, uint32_t e31, uint32_t p31) {
+        row[slot(0)] = (uint16_t)(e31 + p31);
+    }
 
-    static __device__ __forceinline__ void process(const EncodeArgs& a, const uint8_t* table,
-                                                   uint32_t t0, Keep& kp) {
-        const bool full = (uint64_t)t0 + kTileElems <= a.n;
+    // Input words of a full tile: thread t's 32 bytes as two 16-byte loads,
+    // staged at ring slots [0][t] and [1][t].
+    static constexpr int kLoads = 2;
+    static __device__ __forceinline__ const uint8_t* load_src(const EncodeArgs& a, uint32_t t0,
+                                                             int k) {
+        return a.x + t0 + threadIdx.x * 32 + 16 * k;
+    }
+    static __device__ __forceinline__ void compute_full(const EncodeArgs& a, const Tables& tb,
+                                                        uint32_t t0, const uint4 (&v)[kLoads],
+                                                        Keep& kp) {
+        const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+        finish(a, tb.t, t0 + threadIdx.x * 32, w, true, kp);
+    }
+    static __device__ __forceinline__ void process_partial(const EncodeArgs& a, const Tables& tb,
+                                                           uint32_t t0, Keep& kp) {
         const uint32_t i = t0 + threadIdx.x * 32;
-        kp.cnt[0] = 0;
+        kp.cnt = 0;
 #pragma unroll
         for (int m = 0; m < 8; m++) kp.ent[m] = 0;
-        if (!full && i >= a.n) return;
-        const bool whole = full || i + 32 <= a.n;
+        if (i >= a.n) return;
+        const bool whole = i + 32 <= a.n;
         uint32_t w[8];
         if (whole) {
             const uint4 v0 = ld_stream16(a.x + i);
@@ -245,6 +327,14 @@ struct E5m2Dense {
                 w[m] = acc;
             }
         }
+        finish(a, tb.t, i, w, whole, kp);
+    }
+
+    // Fields, codes and stores of the 32 elements at i (input words w).
+    static __device__ __forceinline__ void finish(const EncodeArgs& a, const uint8_t* table,
+                                                  uint32_t i, const uint32_t (&w)[8], bool whole,
+                                                  Keep& kp) {
+        kp.cnt = 0;
         uint32_t f12[8];
 #pragma unroll
         for (int m = 0; m < 8; m++) split_e5m2(w[m], kp.ex[m], f12[m]);
@@ -256,7 +346,7 @@ struct E5m2Dense {
         codes.z = pack_nibbles(kp.ent[4], kp.ent[5]);
         codes.w = pack_nibbles(kp.ent[6], kp.ent[7]);
 #pragma unroll
-        for (int m = 0; m < 8; m += 2) kp.cnt[0] += miss_count(kp.ent[m], kp.ent[m + 1]);
+        for (int m = 0; m < 8; m += 2) kp.cnt += miss_count(kp.ent[m], kp.ent[m + 1]);
         // 8 x 12 bits -> 96 bits, little-endian.
         const uint32_t s0 = f12[0] | (f12[1] << 12) | (f12[2] << 24);
         const uint32_t s1 = (f12[2] >> 8) | (f12[3] << 4) | (f12[4] << 16) | (f12[5] << 28);
@@ -278,12 +368,11 @@ struct E5m2Dense {
         }
     }
 
-    static __device__ __forceinline__ void emit(const Keep& kp, const uint32_t (&rel)[kGroups],
-                                                uint16_t* ent) {
-        if (!kp.cnt[0]) return;
+    static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent) {
+        if (!kp.cnt) return;
         const uint32_t lane = threadIdx.x & 31;
-        uint32_t g = rel[0];
-        uint16_t* e = ent + seg(0) * kSegCap;
+        uint32_t g = excl;
+        uint16_t* e = ent + slot(0) * kSegCap;
 #pragma unroll
         for (int m = 0; m < 8; m++) {
             if (!(kp.ent[m] & 0x10101010u)) continue;
@@ -306,24 +395,60 @@ struct E5m2Dense {
 // --------------------------------------------------------------- K1 dense
 
 // Grid-stride over tiles (one resident wave): the code table is built once
-// per CTA and the tile loop has no barrier at all.
+// per CTA and the tile loop has no barrier at all.  The input of full tiles
+// comes through a per-thread ring of kDenseStages shared-memory slots filled
+// by cp.async: while a thread works on one tile, its copies of the next
+// kDenseStages - 1 tiles are in flight, with no registers held for them.
+// Each thread reads back only the bytes it copied itself, so waiting for its
+// own copy groups is all the synchronisation needed.  A slot is refilled only
+// after the values read from it have been used by the tile's stores.
+constexpr int kDenseStages = 2;
+
+template <class F>
+constexpr size_t dense_smem_bytes() {
+    return (size_t)kDenseStages * F::kLoads * kThreads * sizeof(uint4);
+}
+
 template <class F>
 __global__ void __launch_bounds__(kThreads) dense_kernel(const EncodeArgs a, const MultiPtrs p) {
-    constexpr int G = F::kGroups;
-    __shared__ uint8_t table[256];
-    build_table(table, a.cbw);
-    const uint32_t lane = threadIdx.x & 31;
+    constexpr int L = F::kLoads, S = kDenseStages;
+    extern __shared__ uint4 ring[];  // [S][L][kThreads]
+    __shared__ typename F::Tables tables;
+    F::build_tables(tables, a.cbw);
+    const uint32_t tid = threadIdx.x, lane = tid & 31;
+    const uint32_t full_tiles = a.n / (uint32_t)kTileElems;
+    auto fill = [&](uint32_t tile, int slot) {
+        if (tile < full_tiles) {
+#pragma unroll
+            for (int k = 0; k < L; k++)
+                cp_async16(&ring[(slot * L + k) * kThreads + tid],
+                           F::load_src(a, tile * (uint32_t)kTileElems, k));
+        }
+        cp_async_commit();  // one group per tile, empty for a tile not staged
+    };
+#pragma unroll
+    for (int s = 0; s < S; s++) fill(blockIdx.x + s * gridDim.x, s);
+    int slot = 0;
     for (uint32_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
         const uint32_t t0 = tile * (uint32_t)kTileElems;
         typename F::Keep kp;
-        F::process(a, table, t0, kp);
-        uint32_t rel[G], tot[G];
-        warp_scan<G>(kp.cnt, rel, tot);
+        if (tile < full_tiles) {
+            cp_async_wait<S - 1>();  // this tile's group (the oldest pending) has landed
+            uint4 v[L];
 #pragma unroll
-        for (int g = 0; g < G; g++)
-            if (lane == (uint32_t)g) p.seg_cnt[(size_t)tile * kSegsMax + F::seg(g)] = (uint16_t)tot[g];
-        F::emit(kp, rel, p.seg_ent + (size_t)tile * kEntries);
+            for (int k = 0; k < L; k++) v[k] = ring[(slot * L + k) * kThreads + tid];
+            F::compute_full(a, tables, t0, v, kp);
+        } else {
+            F::process_partial(a, tables, t0, kp);
+        }
+        fill(tile + S * gridDim.x, slot);
+        slot = slot + 1 == S ? 0 : slot + 1;
+        uint32_t excl, e31, p31;
+        warp_scan_excl(kp.cnt, excl, e31, p31);
+        if (lane == 0) F::store_counts(p.seg_cnt + (size_t)tile * kSegsMax, e31, p31);
+        if (kp.cnt) F::emit(kp, excl, p.seg_ent + (size_t)tile * kEntries);
     }
+    cp_async_wait<0>();
 }
 
 // -------------------------------------------------------------- K2 prefix
@@ -450,7 +575,8 @@ __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, con
     const uint32_t len = a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
     const uint32_t q0 = t0 / a.cdiv.d, r0 = t0 - q0 * a.cdiv.d;
     const uint32_t excl = p.tile_excl[tile];
-    const uint32_t cnt = lane < (uint32_t)F::kSegs ? p.seg_cnt[(size_t)tile * kSegsMax + lane] : 0u;
+    const uint32_t cnt =
+        lane < (uint32_t)F::kSegs ? p.seg_cnt[(size_t)tile * kSegsMax + F::storage(lane)] : 0u;
     uint32_t incl = cnt;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -466,7 +592,7 @@ __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, con
         const uint32_t g0 = excl + off;
         if (cnt <= (uint32_t)F::kSegCap) {
             for (uint32_t r = 0; r < cnt; r++) {
-                const uint32_t e = ent[lane * F::kSegCap + r];
+                const uint32_t e = ent[F::storage(lane) * F::kSegCap + r];
                 const uint32_t x = r0 + s0 + (e & kOffMask);
                 put_escape(a, g0 + r, x - chunk_quot(a.cdiv, x) * a.cdiv.d, e >> F::kOffBits);
             }
@@ -498,7 +624,8 @@ __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, con
             const uint32_t lim = bl - sg * F::kSegLen;
             uint32_t rank = 0;
             if (c <= (uint32_t)F::kSegCap) {
-                for (uint32_t r = 0; r < c; r++) rank += (ent[sg * F::kSegCap + r] & kOffMask) < lim;
+                const uint16_t* es = ent + F::storage(sg) * F::kSegCap;
+                for (uint32_t r = 0; r < c; r++) rank += (es[r] & kOffMask) < lim;
             } else {
                 for (uint32_t l = sg * F::kSegLen; l < bl; l++)
                     rank += (table[F::exponent_at(a, t0 + l)] & kMissEntry) != 0;
@@ -518,14 +645,18 @@ cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
     p.seg_ent = reinterpret_cast<uint16_t*>(a.ws + L.seg_ent);
     const uint32_t tiles = a.num_tiles;
     const uint32_t blocks = (tiles + kScanTiles - 1) / kScanTiles;
+    constexpr size_t smem = dense_smem_bytes<F>();
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dense_kernel<F>, kThreads, 0);
+        e = cudaFuncSetAttribute(dense_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dense_kernel<F>, kThreads, smem);
     if (e != cudaSuccess) return e;
     const uint64_t wave = (uint64_t)(sms > 0 ? sms : 1) * (uint64_t)(per_sm > 0 ? per_sm : 1);
-    dense_kernel<F><<<(uint32_t)(tiles < wave ? tiles : wave), kThreads, 0, s>>>(a, p);
+    dense_kernel<F><<<(uint32_t)(tiles < wave ? tiles : wave), kThreads, smem, s>>>(a, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     prefix_kernel<<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks, F::kSegs);
