@@ -48,6 +48,22 @@ class Streams(ctypes.Structure):
                 ("chunk_off", ctypes.c_void_p), ("esc_capacity", ctypes.c_uint64)]
 
 
+class PayloadInfo(ctypes.Structure):
+    _fields_ = [("version", ctypes.c_uint32), ("format", ctypes.c_uint32),
+                ("n", ctypes.c_uint64), ("slice_elems", ctypes.c_uint64),
+                ("num_slices", ctypes.c_uint32), ("chunk_size", ctypes.c_uint32),
+                ("n_escapes", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
+
+
+class SliceEntry(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_uint64), ("n_escapes", ctypes.c_uint64),
+                ("off_dense", ctypes.c_uint64), ("off_escapes", ctypes.c_uint64),
+                ("cb", Codebook)]
+
+
+FORMATS = {"bf16": 0, "e5m2": 1}
+
+
 class EncodeTestOpts(ctypes.Structure):
     _fields_ = [("spin_limit", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
 
@@ -89,6 +105,13 @@ def library() -> ctypes.CDLL:
         "splitzip_decode_e5m2": (st, [sp, u64, u32, cbp, vp, vp]),
         "splitzip_encode_noalloc": (st, [vp, u64, u32, cbp, sp, vp, vp]),
         "splitzip_version": (i32, []),
+        "splitzip_payload_bytes_bound": (u64, [u32, u64, u32, u64, u64]),
+        "splitzip_payload_parse": (st, [vp, u64, ctypes.POINTER(PayloadInfo),
+                                        ctypes.POINTER(SliceEntry), u32]),
+        "splitzip_transfer_scratch_bytes": (ctypes.c_size_t, [u32, u64, u32]),
+        "splitzip_encode_to_host": (st, [vp, u64, u32, u32, cbp, u32, u64, vp, u64,
+                                         ctypes.POINTER(u64), vp, ctypes.c_size_t, vp, vp, vp]),
+        "splitzip_decode_from_host": (st, [vp, u64, vp, u64, vp, ctypes.c_size_t, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -253,6 +276,112 @@ def splitzip_decode(streams: dict, n: int, chunk: int, codebook, y: torch.Tensor
 
 def splitzip_version() -> int:
     return int(library().splitzip_version())
+
+
+# --------------------------------------------------- payloads and transfers
+
+def _ptr(t: torch.Tensor, what: str) -> ctypes.c_void_p:
+    """Pointer of a contiguous tensor on the GPU or in host memory."""
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def splitzip_payload_bytes_bound(n: int, chunk: int, slice_elems: int, n_escapes: int,
+                                 fmt: str = "bf16") -> int:
+    return int(library().splitzip_payload_bytes_bound(FORMATS[fmt], n, chunk, slice_elems,
+                                                      n_escapes))
+
+
+def splitzip_payload_parse(payload: torch.Tensor, nbytes: int | None = None):
+    """(info dict, list of slice dicts) of a host payload; raises if malformed."""
+    if payload.is_cuda or payload.dtype != torch.uint8:
+        raise ValueError("a payload is a host uint8 tensor")
+    nbytes = payload.numel() if nbytes is None else nbytes
+    info = PayloadInfo()
+    _check(library().splitzip_payload_parse(_ptr(payload, "payload"), nbytes, ctypes.byref(info),
+                                            None, 0), "splitzip_payload_parse")
+    entries = (SliceEntry * info.num_slices)()
+    _check(library().splitzip_payload_parse(_ptr(payload, "payload"), nbytes, ctypes.byref(info),
+                                            entries, info.num_slices), "splitzip_payload_parse")
+    d = {k: int(getattr(info, k)) for k, _ in PayloadInfo._fields_}
+    d["fmt"] = {v: k for k, v in FORMATS.items()}[d["format"]]
+    sl = [{"n": int(e.n), "n_escapes": int(e.n_escapes), "off_dense": int(e.off_dense),
+           "off_escapes": int(e.off_escapes), "codebook": list(e.cb.exp)} for e in entries]
+    return d, sl
+
+
+def splitzip_transfer_scratch_bytes(slice_elems: int, chunk: int, fmt: str = "bf16") -> int:
+    return int(library().splitzip_transfer_scratch_bytes(FORMATS[fmt], slice_elems, chunk))
+
+
+def alloc_transfer_scratch(slice_elems: int, chunk: int, fmt: str = "bf16",
+                           device="cuda") -> torch.Tensor:
+    return torch.empty(splitzip_transfer_scratch_bytes(slice_elems, chunk, fmt),
+                       dtype=torch.uint8, device=device)
+
+
+def _cbs(codebooks) -> tuple:
+    """A shared codebook (16 ints) or one codebook per slice."""
+    seq = codebooks.tolist() if hasattr(codebooks, "tolist") else list(codebooks)
+    if len(seq) == 16 and all(isinstance(v, int) for v in seq):
+        seq = [seq]
+    arr = (Codebook * len(seq))()
+    for i, cb in enumerate(seq):
+        arr[i] = _codebook(cb)
+    return arr, len(seq)
+
+
+def _three_streams(streams):
+    if streams is None:
+        raise ValueError("three distinct CUDA streams are needed (compute, h2d, d2h)")
+    return [ctypes.c_void_p(s.cuda_stream) for s in streams]
+
+
+def splitzip_encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems: int,
+                            payload: torch.Tensor, scratch: torch.Tensor, streams,
+                            fmt: str | None = None):
+    """Encode x (GPU or pinned host tensor) slice by slice into the host uint8
+    tensor `payload`.  Returns (status, payload bytes); status is OK or
+    ERR_ESCAPE_OVERFLOW (payload too small: the bytes needed are returned)."""
+    fmt = _fmt_of(x, fmt)
+    arr, k = _cbs(codebooks)
+    nbytes = ctypes.c_uint64()
+    sc, sh, sd = _three_streams(streams)
+    st = library().splitzip_encode_to_host(
+        _ptr(x, "x"), x.numel(), FORMATS[fmt], chunk, arr, k, slice_elems, _ptr(payload, "payload"),
+        payload.numel(), ctypes.byref(nbytes), _dev(scratch, "scratch"), scratch.numel(), sc, sh, sd)
+    if st not in (OK, ERR_ESCAPE_OVERFLOW):
+        _check(st, "splitzip_encode_to_host")
+    return int(st), int(nbytes.value)
+
+
+def splitzip_decode_from_host(payload: torch.Tensor, nbytes: int, y: torch.Tensor,
+                              scratch: torch.Tensor, streams):
+    """Decode a host payload into y (GPU or pinned host tensor); synchronous."""
+    sc, sh, sd = _three_streams(streams)
+    _check(library().splitzip_decode_from_host(
+        _ptr(payload, "payload"), nbytes, _ptr(y, "y"), y.numel(), _dev(scratch, "scratch"),
+        scratch.numel(), sc, sh, sd), "splitzip_decode_from_host")
+
+
+def encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems: int, scratch, streams,
+                   fmt: str | None = None, payload: torch.Tensor | None = None):
+    """splitzip_encode_to_host into a pinned payload, grown once if too small.
+    Returns (payload tensor, payload bytes)."""
+    fmt = _fmt_of(x, fmt)
+    n = x.numel()
+    if payload is None:
+        cap = splitzip_payload_bytes_bound(n, chunk, slice_elems, n // 128 + 4096, fmt)
+        payload = torch.empty(cap, dtype=torch.uint8).pin_memory()
+    st, nbytes = splitzip_encode_to_host(x, chunk, codebooks, slice_elems, payload, scratch,
+                                         streams, fmt)
+    if st == ERR_ESCAPE_OVERFLOW:
+        payload = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        st, nbytes = splitzip_encode_to_host(x, chunk, codebooks, slice_elems, payload, scratch,
+                                             streams, fmt)
+        _check(st, "splitzip_encode_to_host")
+    return payload, nbytes
 
 
 # ------------------------------------------------------------- codec object

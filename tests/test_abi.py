@@ -17,7 +17,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def declared_functions():
     names = set()
-    for h in ("splitzip.h", "splitzip_testing.h"):
+    for h in ("splitzip.h", "splitzip_testing.h", "splitzip_transfer.h"):
         text = open(os.path.join(ROOT, "include", h)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         names |= set(re.findall(r"\b(splitzip_\w+)\s*\(", text))

@@ -1,0 +1,110 @@
+"""Pipelined transfers through host payloads (include/splitzip_transfer.h),
+on the GPU through the C ABI: every payload byte equals the oracle's payload
+of the same slices, and decoding it gives back the input bit for bit, with
+input and output on the device or in pinned host memory."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import payload as op
+from lossless_bf16_kv_gb300 import splitzip as sz
+from lossless_bf16_kv_gb300 import synth
+
+from .gpu_helpers import ensure_library, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _kv(fmt, n, seed):
+    dt = torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2
+    layers = max(1, -(-n // (2 * 256 * 1024)))
+    return synth.kv_cache(layers, 256, seed=seed, device="cuda", dtype=dt).reshape(-1)[:n].clone()
+
+
+def _streams():
+    return [torch.cuda.Stream() for _ in range(3)]
+
+
+def _check_roundtrip(x, fmt, chunk, se, cbs, where):
+    ensure_library()
+    bits = host_bits(x)
+    scratch = sz.alloc_transfer_scratch(se, chunk, fmt)
+    streams = _streams()
+    src = x if where == "device" else x.cpu().pin_memory()
+    payload, nbytes = sz.encode_to_host(src, chunk, cbs, se, scratch, streams, fmt)
+    ref = op.write(bits, fmt, chunk, se, cbs)
+    assert nbytes == len(ref)
+    assert payload[:nbytes].numpy().tobytes() == ref
+    y = torch.empty_like(x)
+    sz.splitzip_decode_from_host(payload, nbytes, y, scratch, streams)
+    assert np.array_equal(host_bits(y), bits)
+    yh = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    sz.splitzip_decode_from_host(payload, nbytes, yh, scratch, streams)
+    assert np.array_equal(host_bits(yh), bits)
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+@pytest.mark.parametrize("fmt,n,chunk,se", [
+    ("bf16", (1 << 20) + 3 * 1024 + 5, 1024, 1 << 18),   # five slices, the last ragged
+    ("bf16", 300000, 256, 65536),
+    ("bf16", 1000, 8, 1024),                              # one slice
+    ("e5m2", (1 << 20) + 77, 1024, 1 << 17),
+    ("e5m2", 50000, 64, 4096),
+])
+def test_transfer_matches_oracle(fmt, n, chunk, se, where):
+    x = _kv(fmt, n, seed=n % 97)
+    cal = _kv(fmt, min(n, 1 << 18), seed=1)
+    cb = [int(c) for c in oracle.calibrate(host_bits(cal), fmt)[0]]
+    _check_roundtrip(x, fmt, chunk, se, cb, where)
+
+
+def test_per_slice_codebooks():
+    fmt, se, chunk = "bf16", 1 << 17, 1024
+    x = _kv(fmt, 5 * se - 100, seed=3)
+    bits = host_bits(x)
+    cbs = [[int(c) for c in oracle.calibrate(bits[i:i + se], fmt)[0]] for i in range(0, x.numel(), se)]
+    _check_roundtrip(x, fmt, chunk, se, cbs, "device")
+
+
+def test_many_escapes():
+    """Student-t values spread over 2^40 of scale: most exponents escape an
+    N(0,1) codebook, so escape regions dominate the payload."""
+    ensure_library()
+    x = synth.student_t_scaled_bf16((512, 1000), seed=4, device="cuda").reshape(-1)
+    cb = [int(c) for c in oracle.calibrate(host_bits(synth.normal_bf16((256, 1024), 1, "cuda")), "bf16")[0]]
+    _check_roundtrip(x, "bf16", 1024, 1 << 16, cb, "device")
+
+
+def test_small_payload_reports_the_size_needed():
+    ensure_library()
+    fmt, chunk, se = "bf16", 1024, 1 << 16
+    x = synth.student_t_scaled_bf16((256, 1024), seed=5, device="cuda").reshape(-1)
+    cb = [int(c) for c in oracle.calibrate(host_bits(synth.normal_bf16((256, 1024), 1, "cuda")), "bf16")[0]]
+    ref = op.write(host_bits(x), fmt, chunk, se, cb)
+    head, _ = op.read(ref)
+    dense_end = min(s["off_escapes"] for s in op.read(ref)[1])
+    scratch, streams = sz.alloc_transfer_scratch(se, chunk, fmt), _streams()
+    small = torch.empty(dense_end + 16, dtype=torch.uint8).pin_memory()
+    st, need = sz.splitzip_encode_to_host(x, chunk, cb, se, small, scratch, streams, fmt)
+    assert st == sz.ERR_ESCAPE_OVERFLOW and need == len(ref) == head["total_bytes"]
+    payload, nbytes = sz.encode_to_host(x, chunk, cb, se, scratch, streams, fmt, payload=small)
+    assert payload[:nbytes].numpy().tobytes() == ref
+
+
+def test_decode_checks_its_arguments():
+    ensure_library()
+    fmt, chunk, se = "bf16", 1024, 1 << 16
+    x = _kv(fmt, 100000, seed=6)
+    cb = [int(c) for c in oracle.calibrate(host_bits(x), fmt)[0]]
+    scratch, streams = sz.alloc_transfer_scratch(se, chunk, fmt), _streams()
+    payload, nbytes = sz.encode_to_host(x, chunk, cb, se, scratch, streams, fmt)
+    y = torch.empty(x.numel() - 1, dtype=x.dtype, device="cuda")
+    with pytest.raises(sz.SplitZipError):
+        sz.splitzip_decode_from_host(payload, nbytes, y, scratch, streams)   # wrong n
+    bad = payload.clone()
+    bad[0] = ord("X")
+    with pytest.raises(sz.SplitZipError):
+        sz.splitzip_decode_from_host(bad, nbytes, torch.empty_like(x), scratch, streams)
+    with pytest.raises(sz.SplitZipError):
+        sz.splitzip_decode_from_host(payload, nbytes, torch.empty_like(x), scratch[:1024], streams)
