@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -84,15 +85,20 @@ def measured_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Sources of the kernels the bench times (encode passes, decode) and what they
+# include; host-only files (the C ABI, transfers) do not change the kernels.
+KERNEL_SOURCES = ("encode_multi.cu", "decode.cu", "common.cuh", "fields.cuh", "kernels.h",
+                  "lookback.cuh")
+
+
 def kernel_source_sha() -> str:
-    """Hash of the kernel sources; a stored ncu traffic figure is used only
-    while it matches (a changed kernel makes the figure stale)."""
+    """Hash of the timed kernels' sources; a stored ncu traffic figure is used
+    only while it matches (a changed kernel makes the figure stale)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lossless_bf16_kv_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -278,7 +284,11 @@ def run_gpu(args):
         "algo_bytes": algorithmic_bytes(fmt, n, chunk, E), "elem": elem,
     }
     if args.e2e:
-        res["e2e"] = run_e2e(x, y, streams, ws, cb, fmt, chunk, E, K, dev, world)
+        del streams, y
+        torch.cuda.empty_cache()
+        res["e2e"] = run_e2e(x, cb, fmt, chunk, K, dev, world)
+        if rank == 0 and world == 1:
+            res["transfer"] = run_transfer(x, cb, fmt, chunk, dev)
     if rank == 0 and world == 1 and args.cpu_baseline:
         res["cpu_sample"] = synth.raw_bits(x[: min(n, args.cpu_sample_elems)]).cpu()
     if world > 1:
@@ -286,48 +296,108 @@ def run_gpu(args):
     return res
 
 
-def run_e2e(x, y, streams, ws, cb, fmt, chunk, E, K, dev, world):
-    """The same step through the public C ABI with the tensor in pinned host
-    memory: host->device copy of the input, encode, decode, device->host copy
-    of the decoded tensor, all inside the timed region."""
+def transfer_slice_elems(n: int, chunk: int) -> int:
+    """Slice size of the pipelined transfers: one KV-cache layer (2 x 16384 x
+    8 x 128 elements) of the prefill workloads, or the whole tensor rounded up
+    to chunk and 16-element multiples when smaller."""
+    unit = chunk * 16 // math.gcd(chunk, 16)
+    return min(1 << 25, -(-n // unit) * unit)
+
+
+def run_e2e(x, cb, fmt, chunk, K, dev, world):
+    """The step through the public C ABI with host buffers: the tensor in
+    pinned host memory is encoded into a host payload (splitzip_encode_to_host:
+    slice copies to the device, encode, streams back), and the payload decoded
+    into pinned host memory (splitzip_decode_from_host), copies overlapping the
+    kernels.  Timed on the host clock around synchronous calls that span three
+    streams."""
     import torch
     import torch.distributed as dist
 
     from lossless_bf16_kv_gb300 import splitzip as sz
 
-    n = x.numel()
-    hx = torch.empty_like(x, device="cpu").pin_memory()
-    hy = torch.empty_like(y, device="cpu").pin_memory()
+    n, eb = x.numel(), x.element_size()
+    se = transfer_slice_elems(n, chunk)
+    hx = torch.empty(n, dtype=x.dtype).pin_memory()
     hx.copy_(x)
-    steps = max(1, min(K, 20))
+    hy = torch.empty_like(hx).pin_memory()
+    scratch = sz.alloc_transfer_scratch(se, chunk, fmt, dev)
+    streams = [torch.cuda.Stream(dev) for _ in range(3)]
+    payload, nbytes = sz.encode_to_host(hx, chunk, cb, se, scratch, streams, fmt)
+    steps = max(1, min(K, 10))
 
     def step():
-        x.copy_(hx, non_blocking=True)
-        sz.splitzip_encode(x, chunk, cb, streams, ws, fmt)
-        sz.splitzip_decode(streams, n, chunk, cb, y, fmt, n_escapes=E)
-        hy.copy_(y, non_blocking=True)
+        st, nb = sz.splitzip_encode_to_host(hx, chunk, cb, se, payload, scratch, streams, fmt)
+        assert st == sz.OK and nb == nbytes
+        sz.splitzip_decode_from_host(payload, nbytes, hy, scratch, streams)
 
     for _ in range(2):
         step()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
+    t0 = time.perf_counter()
     for _ in range(steps):
         step()
-    t1.record()
     torch.cuda.synchronize()
-    secs = t0.elapsed_time(t1) / 1e3
+    secs = time.perf_counter() - t0
     if world > 1:
         tt = torch.tensor([secs], dtype=torch.float64, device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         secs = tt.item()
     if not torch.equal(hx, hy):
         _fail("end-to-end round trip is not bit-exact")
-    nbytes = x.numel() * x.element_size()
-    return {"value": round(nbytes * steps * world / secs / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": steps}
+    raw = n * eb
+    return {"value": round(raw * steps * world / secs / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": raw + nbytes, "d2h_bytes_per_step": nbytes + raw,
+            "steps": steps, "slice_elems": se, "payload_bytes": nbytes,
+            "path": "pinned host tensor -> splitzip_encode_to_host -> host payload -> "
+                    "splitzip_decode_from_host -> pinned host tensor (host clock)"}
+
+
+def run_transfer(x, cb, fmt, chunk, dev):
+    """KV transfer over the host link, the codec's use on the pages: a device
+    tensor to a host payload and back to the device (splitzip_encode_to_host,
+    splitzip_decode_from_host), against moving the raw bytes device -> host ->
+    device with one copy each way.  Best of three, host clock."""
+    import torch
+
+    from lossless_bf16_kv_gb300 import splitzip as sz
+
+    n, eb = x.numel(), x.element_size()
+    se = transfer_slice_elems(n, chunk)
+    scratch = sz.alloc_transfer_scratch(se, chunk, fmt, dev)
+    streams = [torch.cuda.Stream(dev) for _ in range(3)]
+    payload, nbytes = sz.encode_to_host(x, chunk, cb, se, scratch, streams, fmt)
+    y = torch.empty_like(x)
+    h = torch.empty(n, dtype=x.dtype).pin_memory()
+
+    def best(fn):
+        t = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            t.append(time.perf_counter() - t0)
+        return min(t)
+
+    enc = best(lambda: sz.splitzip_encode_to_host(x, chunk, cb, se, payload, scratch, streams, fmt))
+    dec = best(lambda: sz.splitzip_decode_from_host(payload, nbytes, y, scratch, streams))
+    if not torch.equal(synth_bits(x), synth_bits(y)):
+        _fail("transfer round trip is not bit-exact")
+    d2h = best(lambda: h.copy_(x, non_blocking=True))
+    h2d = best(lambda: y.copy_(h, non_blocking=True))
+    return {"raw_ms": round((d2h + h2d) * 1e3, 3), "splitzip_ms": round((enc + dec) * 1e3, 3),
+            "speedup": round((d2h + h2d) / (enc + dec), 4),
+            "encode_to_host_ms": round(enc * 1e3, 3), "decode_from_host_ms": round(dec * 1e3, 3),
+            "raw_bytes": n * eb, "payload_bytes": nbytes, "slice_elems": se,
+            "path": "device tensor -> host payload -> device tensor, vs raw device -> host -> device"}
+
+
+def synth_bits(t):
+    from lossless_bf16_kv_gb300 import synth
+    return synth.raw_bits(t)
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -502,6 +572,8 @@ def main():
     }
     if "e2e" in res:
         line["e2e"] = res["e2e"]
+    if "transfer" in res:
+        line["transfer"] = res["transfer"]
     if "cpu_sample" in res:
         line["cpu_baseline"] = cpu_baseline(res["cpu_sample"], res["fmt"], res["chunk"],
                                             res["codebook"], args.cpu_seconds)
