@@ -142,6 +142,18 @@ splitzip_status splitzip_calibrate_async_e5m2(const void *d_x, uint64_t n, uint8
                                               uint64_t *d_covered_out, void *d_workspace,
                                               splitzip_stream_t s);
 
+/* The exponent histogram of the n elements at d_x (16-byte aligned) into
+ * DEVICE memory: d_hist_out (8-byte aligned) receives 256 (BF16) or 32 (E5M2)
+ * uint64 counts, bin e = elements whose exponent is e.  The same kernel as
+ * calibration (the pages' calibration step starts from this histogram; it
+ * also feeds exponent-entropy and top-k coverage reports).  Asynchronous on
+ * s; uses the workspace like splitzip_calibrate_async.
+ * 1 <= n <= SPLITZIP_MAX_ELEMENTS. */
+splitzip_status splitzip_histogram(const void* d_x, uint64_t n, uint64_t* d_hist_out,
+                                   void* d_workspace, splitzip_stream_t s);
+splitzip_status splitzip_histogram_e5m2(const void* d_x, uint64_t n, uint64_t* d_hist_out,
+                                        void* d_workspace, splitzip_stream_t s);
+
 /* --------------------------------------------------------------- encode */
 
 /* Encode n elements at d_x (16-byte aligned; BF16 or E5M2 bit patterns) with

@@ -129,6 +129,24 @@ splitzip_status calibrate_async_impl(const void* d_x, uint64_t n, uint8_t* d_cb,
     a.ws = static_cast<uint8_t*>(ws);
     a.cb_out = d_cb;
     a.covered_out = d_covered;
+    a.hist_out = nullptr;
+    return from_cuda(launch_calibrate(a, e5m2, s));
+}
+
+splitzip_status histogram_impl(const void* d_x, uint64_t n, uint64_t* d_hist, void* ws,
+                               cudaStream_t s, bool e5m2) {
+    if (!d_x || !d_hist || !ws) return SPLITZIP_ERR_INVALID_ARG;
+    if (!count_ok(n)) return SPLITZIP_ERR_INVALID_ARG;
+    if (!aligned(d_x, 16) || !aligned(d_hist, 8) || !aligned(ws, 16)) return SPLITZIP_ERR_INVALID_ARG;
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    CalibArgs a;
+    a.x = static_cast<const uint8_t*>(d_x);
+    a.n = (uint32_t)n;
+    a.grid = calibrate_grid((uint32_t)n, num_sms_current());
+    a.ws = static_cast<uint8_t*>(ws);
+    a.cb_out = hdr->cal_cb;  // the codebook and coverage land in the workspace, unused
+    a.covered_out = &hdr->cal_covered;
+    a.hist_out = d_hist;
     return from_cuda(launch_calibrate(a, e5m2, s));
 }
 
@@ -207,6 +225,16 @@ splitzip_status splitzip_calibrate_async_e5m2(const void* d_x, uint64_t n, uint8
                                               splitzip_stream_t s) {
     return calibrate_async_impl(d_x, n, d_cb_out, d_covered_out, d_workspace, (cudaStream_t)s,
                                 true);
+}
+
+splitzip_status splitzip_histogram(const void* d_x, uint64_t n, uint64_t* d_hist_out,
+                                   void* d_workspace, splitzip_stream_t s) {
+    return histogram_impl(d_x, n, d_hist_out, d_workspace, (cudaStream_t)s, false);
+}
+
+splitzip_status splitzip_histogram_e5m2(const void* d_x, uint64_t n, uint64_t* d_hist_out,
+                                        void* d_workspace, splitzip_stream_t s) {
+    return histogram_impl(d_x, n, d_hist_out, d_workspace, (cudaStream_t)s, true);
 }
 
 splitzip_status splitzip_encode(const void* d_x, uint64_t n, uint32_t chunk_size,

@@ -10,8 +10,8 @@
 // not contend), folds them and adds them into the workspace's global
 // histogram.  The last CTA to finish (an atomic counter) ranks the bins by
 // (count descending, exponent ascending), writes the first 16 as the
-// codebook together with the covered count, and zeroes the global histogram
-// for the next launch.
+// codebook together with the covered count (and, when asked, the whole
+// histogram), and zeroes the global histogram for the next launch.
 #include <cstdint>
 
 #include "common.cuh"
@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kThreads) calibrate_kernel(const CalibArgs a) 
     }
     __syncthreads();
     if (tid < 16) a.cb_out[tid] = s_cb[tid];
+    if (a.hist_out && tid < kBins) a.hist_out[tid] = s_cnt[tid];
     if (tid == 0) {
         unsigned long long covered = 0;
         for (int k = 0; k < 16; k++) covered += s_cnt[s_cb[k]];

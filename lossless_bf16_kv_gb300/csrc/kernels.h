@@ -54,6 +54,7 @@ struct CalibArgs {
     uint8_t* ws;
     uint8_t* cb_out;        // 16 bytes, device
     uint64_t* covered_out;  // device
+    uint64_t* hist_out;     // device, 256 (BF16) / 32 (E5M2) counts, or null
 };
 
 // Workspace layout of the multi-kernel encode, all offsets from the workspace

@@ -96,6 +96,8 @@ def library() -> ctypes.CDLL:
         "splitzip_calibrate_e5m2": (st, [vp, u64, cbp, ctypes.POINTER(ctypes.c_double), vp, vp]),
         "splitzip_calibrate_async": (st, [vp, u64, vp, vp, vp, vp]),
         "splitzip_calibrate_async_e5m2": (st, [vp, u64, vp, vp, vp, vp]),
+        "splitzip_histogram": (st, [vp, u64, vp, vp, vp]),
+        "splitzip_histogram_e5m2": (st, [vp, u64, vp, vp, vp]),
         "splitzip_encode": (st, [vp, u64, u32, cbp, sp, vp, vp]),
         "splitzip_encode_e5m2": (st, [vp, u64, u32, cbp, sp, vp, vp]),
         "splitzip_encode_test": (st, [vp, u64, u32, cbp, sp, vp, vp, i32,
@@ -229,6 +231,19 @@ def splitzip_calibrate_async(x: torch.Tensor, cb_out: torch.Tensor, covered_out:
           else library().splitzip_calibrate_async_e5m2)
     _check(fn(_dev(x, "x"), x.numel(), _dev(cb_out, "cb_out"), _dev(covered_out, "covered_out"),
               _dev(workspace, "workspace"), _stream(stream)), "splitzip_calibrate_async")
+
+
+def splitzip_histogram(x: torch.Tensor, workspace: torch.Tensor, fmt: str | None = None,
+                       stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Exponent histogram of x on the GPU: int64 tensor of 256 (BF16) / 32 (E5M2)
+    counts; asynchronous."""
+    fmt = _fmt_of(x, fmt)
+    if out is None:
+        out = torch.empty(256 if fmt == "bf16" else 32, dtype=torch.int64, device=x.device)
+    fn = library().splitzip_histogram if fmt == "bf16" else library().splitzip_histogram_e5m2
+    _check(fn(_dev(x, "x"), x.numel(), _dev(out, "out"), _dev(workspace, "workspace"),
+              _stream(stream)), "splitzip_histogram")
+    return out
 
 
 def splitzip_encode(x: torch.Tensor, chunk: int, codebook, streams: dict,
