@@ -13,9 +13,9 @@
 //                communication: input staged through a per-thread cp.async
 //                ring, field split, code lookup in shared-memory word tables,
 //                dense code and sign+mantissa stores.  Each warp ranks the
-//                escapes of its segments with one shuffle scan and stores the
-//                counts and the first few escapes of every segment in the
-//                workspace.
+//                escapes of its segments (ballots when no group holds two
+//                escapes, else one shuffle scan) and stores the counts and
+//                the first few escapes of every segment in the workspace.
 //   K2 prefix    exclusive prefix of the per-tile escape counts (sums of the
 //                segment counts; 2048 tiles per CTA,
 //                decoupled look-back across CTAs, bounded waits); E.
@@ -95,9 +95,7 @@ __device__ __forceinline__ void warp_scan_excl(uint32_t p, uint32_t& excl, uint3
 //   T_j[e] = 1 << (16 + j)          for an escape (code 0, flag bit).
 // The four entries of elements 4h..4h+3 occupy disjoint bits, so their sum is
 // the half group's four code nibbles (bits 0..15) and escape flags (bits
-// 16..19).  The sign+mantissa byte of a value is the sum of its masked low
-// byte (mantissa) and high byte (sign): (w & 0x807F807F) * 257 leaves both
-// values' bytes in bytes 1 and 3 of the product, with no carries.
+// 16..19).
 struct Bf16Dense {
     static constexpr int kGroups = 4;
     static constexpr int kSegs = 32;
@@ -156,9 +154,12 @@ struct Bf16Dense {
     // Codes, sign+mantissa bytes and escape flags of the 8 values in v.
     static __device__ __forceinline__ void group(const Tables& tb, const uint4& v, uint32_t& codes,
                                                  uint2& sm, uint32_t& miss) {
-        const uint32_t u0 = (v.x & 0x807F807Fu) * 257u, u1 = (v.y & 0x807F807Fu) * 257u;
-        const uint32_t u2 = (v.z & 0x807F807Fu) * 257u, u3 = (v.w & 0x807F807Fu) * 257u;
-        sm = make_uint2(__byte_perm(u0, u1, 0x7531), __byte_perm(u2, u3, 0x7531));
+        // Low and high bytes of four values each; sign from the high byte, mantissa
+        // from the low byte.
+        const uint32_t lo0 = __byte_perm(v.x, v.y, 0x6420), hi0 = __byte_perm(v.x, v.y, 0x7531);
+        const uint32_t lo1 = __byte_perm(v.z, v.w, 0x6420), hi1 = __byte_perm(v.z, v.w, 0x7531);
+        sm = make_uint2((hi0 & 0x80808080u) | (lo0 & 0x7F7F7F7Fu),
+                        (hi1 & 0x80808080u) | (lo1 & 0x7F7F7F7Fu));
         const uint32_t A = ent_lo(tb, 0, v.x) + ent_hi(tb, 1, v.x) + ent_lo(tb, 2, v.y) + ent_hi(tb, 3, v.y);
         const uint32_t B = ent_lo(tb, 0, v.z) + ent_hi(tb, 1, v.z) + ent_lo(tb, 2, v.w) + ent_hi(tb, 3, v.w);
         codes = __byte_perm(A, B, 0x5410);
@@ -168,13 +169,17 @@ struct Bf16Dense {
     // Input words of a full tile: load k of thread t is the 16 bytes of its
     // group k, staged at ring slot [k][t].
     static constexpr int kLoads = kGroups;
+    static constexpr bool kSharedStage = false;  // each thread reads back only its own copies
     static __device__ __forceinline__ const uint8_t* load_src(const EncodeArgs& a, uint32_t t0,
                                                              int k) {
         return a.x + 2ull * (t0 + loff(k));
     }
+    static __device__ __forceinline__ uint32_t load_slot(int k) { return k * kThreads + threadIdx.x; }
     static __device__ __forceinline__ void compute_full(const EncodeArgs& a, const Tables& tb,
-                                                        uint32_t t0, const uint4 (&v)[kLoads],
-                                                        Keep& kp) {
+                                                        uint32_t t0, const uint4* stage, Keep& kp) {
+        uint4 v[kLoads];
+#pragma unroll
+        for (int k = 0; k < kLoads; k++) v[k] = stage[load_slot(k)];
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
             const uint32_t i = t0 + loff(k);
@@ -232,6 +237,31 @@ struct Bf16Dense {
         }
     }
 
+    // True when one of this lane's groups holds two or more escapes.
+    static __device__ __forceinline__ bool multi(const Keep& kp) {
+        return (kp.cnt & 0xFEFEFEFEu) != 0;
+    }
+    // Counts and escapes when no group of the warp holds more than one escape
+    // (almost every tile at KV-cache escape rates): a group's rank is the
+    // number of lower lanes whose same group has an escape, a segment's total
+    // the population of that ballot.
+    static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
+                                                           uint16_t* ent) {
+        const uint32_t lane = threadIdx.x & 31, lt = (1u << lane) - 1u;
+        uint32_t has[kGroups];
+#pragma unroll
+        for (int k = 0; k < kGroups; k++) has[k] = __ballot_sync(0xFFFFFFFFu, kp.miss[k] != 0);
+        if (lane == 0)
+            *reinterpret_cast<uint2*>(row + slot(0)) =
+                make_uint2(__popc(has[0]) | (__popc(has[1]) << 16), __popc(has[2]) | (__popc(has[3]) << 16));
+        if (kp.cnt) {
+            uint32_t excl = 0;
+#pragma unroll
+            for (int k = 0; k < kGroups; k++) excl |= (uint32_t)__popc(has[k] & lt) << (8 * k);
+            emit(kp, excl, ent);
+        }
+    }
+
     // The first kSegCap escapes of each segment into its workspace entries.
     // excl: the exclusive escape ranks of this lane's groups, one per byte.
     static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent) {
@@ -286,17 +316,24 @@ struct E5m2Dense {
         row[slot(0)] = (uint16_t)(e31 + p31);
     }
 
-    // Input words of a full tile: thread t's 32 bytes as two 16-byte loads,
-    // staged at ring slots [0][t] and [1][t].
+    // Input words of a full tile.  Warp w's 1 KiB (elements 1024w..1024w+1023)
+    // arrives as 64 pieces of 16 bytes, lane l copying pieces l and 32 + l of
+    // it (coalesced), into stage slots [64w + piece]; thread t then reads its
+    // own 32 bytes (pieces 2l and 2l + 1) after a __syncwarp.
     static constexpr int kLoads = 2;
+    static constexpr bool kSharedStage = true;  // lanes read pieces other lanes copied
     static __device__ __forceinline__ const uint8_t* load_src(const EncodeArgs& a, uint32_t t0,
                                                              int k) {
-        return a.x + t0 + threadIdx.x * 32 + 16 * k;
+        return a.x + t0 + 1024 * (threadIdx.x >> 5) + 512 * k + 16 * (threadIdx.x & 31);
+    }
+    static __device__ __forceinline__ uint32_t load_slot(int k) {
+        return 64 * (threadIdx.x >> 5) + 32 * k + (threadIdx.x & 31);
     }
     static __device__ __forceinline__ void compute_full(const EncodeArgs& a, const Tables& tb,
-                                                        uint32_t t0, const uint4 (&v)[kLoads],
-                                                        Keep& kp) {
-        const uint32_t w[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+                                                        uint32_t t0, const uint4* stage, Keep& kp) {
+        const uint32_t base = 64 * (threadIdx.x >> 5) + 2 * (threadIdx.x & 31);
+        const uint4 v0 = stage[base], v1 = stage[base + 1];
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         finish(a, tb.t, t0 + threadIdx.x * 32, w, true, kp);
     }
     static __device__ __forceinline__ void process_partial(const EncodeArgs& a, const Tables& tb,
@@ -368,6 +405,16 @@ struct E5m2Dense {
         }
     }
 
+    static __device__ __forceinline__ bool multi(const Keep& kp) { return kp.cnt >= 2; }
+    // Counts and escapes when no lane of the warp holds more than one escape.
+    static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
+                                                           uint16_t* ent) {
+        const uint32_t lane = threadIdx.x & 31;
+        const uint32_t has = __ballot_sync(0xFFFFFFFFu, kp.cnt != 0);
+        if (lane == 0) row[slot(0)] = (uint16_t)__popc(has);
+        if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent);
+    }
+
     static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent) {
         if (!kp.cnt) return;
         const uint32_t lane = threadIdx.x & 31;
@@ -421,7 +468,7 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(const EncodeArgs a, con
         if (tile < full_tiles) {
 #pragma unroll
             for (int k = 0; k < L; k++)
-                cp_async16(&ring[(slot * L + k) * kThreads + tid],
+                cp_async16(&ring[slot * L * kThreads + F::load_slot(k)],
                            F::load_src(a, tile * (uint32_t)kTileElems, k));
         }
         cp_async_commit();  // one group per tile, empty for a tile not staged
@@ -434,19 +481,24 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(const EncodeArgs a, con
         typename F::Keep kp;
         if (tile < full_tiles) {
             cp_async_wait<S - 1>();  // this tile's group (the oldest pending) has landed
-            uint4 v[L];
-#pragma unroll
-            for (int k = 0; k < L; k++) v[k] = ring[(slot * L + k) * kThreads + tid];
-            F::compute_full(a, tables, t0, v, kp);
+            if (F::kSharedStage) __syncwarp();  // the warp's copies, visible to all its lanes
+            F::compute_full(a, tables, t0, ring + slot * L * kThreads, kp);
         } else {
             F::process_partial(a, tables, t0, kp);
         }
+        if (F::kSharedStage) __syncwarp();  // every lane has read the stage before the refill
         fill(tile + S * gridDim.x, slot);
         slot = slot + 1 == S ? 0 : slot + 1;
-        uint32_t excl, e31, p31;
-        warp_scan_excl(kp.cnt, excl, e31, p31);
-        if (lane == 0) F::store_counts(p.seg_cnt + (size_t)tile * kSegsMax, e31, p31);
-        if (kp.cnt) F::emit(kp, excl, p.seg_ent + (size_t)tile * kEntries);
+        uint16_t* row = p.seg_cnt + (size_t)tile * kSegsMax;
+        uint16_t* ent = p.seg_ent + (size_t)tile * kEntries;
+        if (!__any_sync(0xFFFFFFFFu, F::multi(kp))) {
+            F::bookkeep_single(kp, row, ent);
+        } else {
+            uint32_t excl, e31, p31;
+            warp_scan_excl(kp.cnt, excl, e31, p31);
+            if (lane == 0) F::store_counts(row, e31, p31);
+            if (kp.cnt) F::emit(kp, excl, ent);
+        }
     }
     cp_async_wait<0>();
 }
