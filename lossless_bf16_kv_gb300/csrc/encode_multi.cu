@@ -172,7 +172,9 @@ struct Bf16Dense {
     static constexpr bool kSharedStage = false;  // each thread reads back only its own copies
     static __device__ __forceinline__ const uint8_t* load_src(const EncodeArgs& a, uint32_t t0,
                                                              int k) {
-        return a.x + 2ull * (t0 + loff(k));
+        // One 64-bit base per tile and constant group offsets (a 32-bit element
+        // index per group would cost an add and a widening add per access).
+        return a.x + 2ull * (t0 + threadIdx.x * 8) + (uint32_t)(k * kThreads * 16);
     }
     static __device__ __forceinline__ uint32_t load_slot(int k) { return k * kThreads + threadIdx.x; }
     static __device__ __forceinline__ void compute_full(const EncodeArgs& a, const Tables& tb,
@@ -180,16 +182,18 @@ struct Bf16Dense {
         uint4 v[kLoads];
 #pragma unroll
         for (int k = 0; k < kLoads; k++) v[k] = stage[load_slot(k)];
+        const uint32_t i0 = t0 + threadIdx.x * 8;  // group 0's first element
+        uint8_t* cbase = a.codes + i0 / 2;
+        uint8_t* sbase = a.signman + i0;
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
-            const uint32_t i = t0 + loff(k);
             uint32_t codes, miss;
             uint2 sm;
             group(tb, v[k], codes, sm, miss);
             kp.v[k] = v[k];
             kp.miss[k] = miss;
-            st_stream4(a.codes + i / 2, codes);
-            st_stream8(a.signman + i, sm);
+            st_stream4(cbase + k * (kThreads * 4), codes);
+            st_stream8(sbase + k * (kThreads * 8), sm);
         }
         kp.cnt = __popc(kp.miss[0]) | (__popc(kp.miss[1]) << 8) | (__popc(kp.miss[2]) << 16) |
                  (__popc(kp.miss[3]) << 24);
