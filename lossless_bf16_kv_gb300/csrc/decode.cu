@@ -205,6 +205,7 @@ __device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* sm
                     (size_t)warp * F::kExWords * 32;
     uint32_t seg = blockIdx.x * kWarps + warp;
     if (seg >= nseg) return;  // warp-uniform
+    const uint64_t pol = l2_evict_first_policy();  // the streams are read once
 
     // Lanes copy the segment's dense bytes 16 at a time; a lane may read bytes
     // another lane copied, so every read of a stage follows this lane's wait
@@ -221,7 +222,7 @@ __device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* sm
                     const uint8_t* src = off < (uint32_t)F::kCodeBytes
                                              ? a.codes + s0 / 2 + off
                                              : a.signman + F::sm_offset(s0) + (off - F::kCodeBytes);
-                    cp_async16(dst + off, src);
+                    cp_async16_hint(dst + off, src, pol);
                 }
             }
         }
