@@ -19,7 +19,8 @@
 //   K2 prefix    exclusive prefix of the per-tile escape counts (sums of the
 //                segment counts; 2048 tiles per CTA,
 //                decoupled look-back across CTAs, bounded waits); E.
-//   K3 place     a warp per tile: segment offsets by shuffle scan, escapes
+//   K3 place     a warp per tile (BF16) or four (E5M2): segment offsets by
+//                shuffle scan, escapes
 //                copied to their final places, chunk offsets at chunk starts.
 //                A segment with more escapes than its workspace share is
 //                rebuilt from the input in element order.
@@ -618,37 +619,44 @@ __device__ __forceinline__ void put_escape(const EncodeArgs& a, uint32_t g, uint
     }
 }
 
+// A warp places the escapes of 32 / kSegs consecutive tiles (BF16: one, E5M2:
+// four), lane l taking segment l mod kSegs (element order) of tile l / kSegs.
 template <class F>
 __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, const MultiPtrs p,
                                                          uint32_t num_tiles) {
     constexpr uint32_t kOffMask = (1u << F::kOffBits) - 1u;
+    constexpr uint32_t SEGS = F::kSegs, TPW = 32 / F::kSegs;
     __shared__ uint8_t table[256];
     build_table(table, a.cbw);
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t tile = blockIdx.x * kWarps + warp;
-    if (tile >= num_tiles) return;  // warp-uniform
+    const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW;
+    if (tile0 >= num_tiles) return;  // warp-uniform
+    const uint32_t sub = lane / SEGS, sgl = lane % SEGS;  // this lane's tile and segment
+    const uint32_t tile = tile0 + sub;
+    const bool tvalid = tile < num_tiles;
     const uint32_t t0 = tile * (uint32_t)kTileElems;
-    const uint32_t len = a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
-    const uint32_t q0 = t0 / a.cdiv.d, r0 = t0 - q0 * a.cdiv.d;
-    const uint32_t excl = p.tile_excl[tile];
-    const uint32_t cnt =
-        lane < (uint32_t)F::kSegs ? p.seg_cnt[(size_t)tile * kSegsMax + F::storage(lane)] : 0u;
+    const uint32_t len = !tvalid ? 0u : a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
+    const uint32_t q0 = chunk_quot32(a.cdiv, t0), r0 = t0 - q0 * a.cdiv.d;
+    const uint32_t excl = tvalid ? p.tile_excl[tile] : 0u;
+    const uint32_t cnt = tvalid ? p.seg_cnt[(size_t)tile * kSegsMax + F::storage(sgl)] : 0u;
+    // Exclusive scan of the counts within each tile's group of SEGS lanes.
     uint32_t incl = cnt;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += u;
+        if (lane >= (uint32_t)d) incl += u;
     }
-    const uint32_t off = incl - cnt;
+    const uint32_t first = __shfl_sync(0xFFFFFFFFu, incl - cnt, lane & ~(SEGS - 1));
+    const uint32_t off = incl - cnt - first;
     const uint16_t* ent = p.seg_ent + (size_t)tile * kEntries;
 
-    // Escapes of segment `lane`, in element order.
+    // Escapes of segment sgl of this lane's tile, in element order.
     if (cnt) {
-        const uint32_t s0 = lane * F::kSegLen;
+        const uint32_t s0 = sgl * F::kSegLen;
         const uint32_t g0 = excl + off;
         if (cnt <= (uint32_t)F::kSegCap) {
             for (uint32_t r = 0; r < cnt; r++) {
-                const uint32_t e = ent[F::storage(lane) * F::kSegCap + r];
+                const uint32_t e = ent[F::storage(sgl) * F::kSegCap + r];
                 const uint32_t x = r0 + s0 + (e & kOffMask);
                 put_escape(a, g0 + r, x - chunk_quot(a.cdiv, x) * a.cdiv.d, e >> F::kOffBits);
             }
@@ -666,27 +674,37 @@ __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, con
         }
     }
 
-    // chunk_off at every chunk start in the tile: the exclusive escape rank of
-    // the chunk's first element.
-    const uint32_t qa = r0 ? 1u : 0u, qb = chunk_quot(a.cdiv, r0 + len - 1);
-    for (uint32_t b0 = qa; b0 <= qb; b0 += 32) {
-        const uint32_t q = b0 + lane;
-        const bool valid = q <= qb;
-        const uint32_t bl = valid ? q * a.cdiv.d - r0 : 0u;  // tile-local index of the chunk start
-        const uint32_t sg = bl / F::kSegLen;
-        const uint32_t o = __shfl_sync(0xFFFFFFFFu, off, sg);
-        const uint32_t c = __shfl_sync(0xFFFFFFFFu, cnt, sg);
-        if (valid) {
-            const uint32_t lim = bl - sg * F::kSegLen;
-            uint32_t rank = 0;
-            if (c <= (uint32_t)F::kSegCap) {
-                const uint16_t* es = ent + F::storage(sg) * F::kSegCap;
-                for (uint32_t r = 0; r < c; r++) rank += (es[r] & kOffMask) < lim;
-            } else {
-                for (uint32_t l = sg * F::kSegLen; l < bl; l++)
-                    rank += (table[F::exponent_at(a, t0 + l)] & kMissEntry) != 0;
+    // chunk_off at every chunk start of each of the warp's tiles: the exclusive
+    // escape rank of the chunk's first element.
+    for (uint32_t t = 0; t < TPW; t++) {
+        const uint32_t tl = tile0 + t;
+        if (tl >= num_tiles) break;  // warp-uniform
+        const uint32_t u0 = tl * (uint32_t)kTileElems;
+        const uint32_t ulen = a.n - u0 < (uint32_t)kTileElems ? a.n - u0 : (uint32_t)kTileElems;
+        const uint32_t uq0 = chunk_quot32(a.cdiv, u0), ur0 = u0 - uq0 * a.cdiv.d;
+        const uint32_t uexcl = __shfl_sync(0xFFFFFFFFu, excl, t * SEGS);
+        const uint16_t* uent = p.seg_ent + (size_t)tl * kEntries;
+        const uint32_t qa = ur0 ? 1u : 0u, qb = chunk_quot(a.cdiv, ur0 + ulen - 1);
+        for (uint32_t b0 = qa; b0 <= qb; b0 += 32) {
+            const uint32_t q = b0 + lane;
+            const bool valid = q <= qb;
+            const uint32_t bl = valid ? q * a.cdiv.d - ur0 : 0u;  // tile-local index of the chunk start
+            const uint32_t sg = bl / F::kSegLen;
+            const uint32_t o = __shfl_sync(0xFFFFFFFFu, off, t * SEGS + sg);
+            const uint32_t c = __shfl_sync(0xFFFFFFFFu, cnt, t * SEGS + sg);
+            if (valid) {
+                const uint32_t lim = bl - sg * F::kSegLen;
+                uint32_t rank = 0;
+                if (lim == 0) {
+                } else if (c <= (uint32_t)F::kSegCap) {
+                    const uint16_t* es = uent + F::storage(sg) * F::kSegCap;
+                    for (uint32_t r = 0; r < c; r++) rank += (es[r] & kOffMask) < lim;
+                } else {
+                    for (uint32_t l = sg * F::kSegLen; l < bl; l++)
+                        rank += (table[F::exponent_at(a, u0 + l)] & kMissEntry) != 0;
+                }
+                a.chunk_off[uq0 + q] = uexcl + o + rank;
             }
-            a.chunk_off[q0 + q] = excl + o + rank;
         }
     }
 }
@@ -718,7 +736,8 @@ cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
     prefix_kernel<<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks, F::kSegs);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    place_kernel<F><<<(tiles + kWarps - 1) / kWarps, kThreads, 0, s>>>(a, p, tiles);
+    const uint32_t per_cta = kWarps * (32 / F::kSegs);  // tiles per placement CTA
+    place_kernel<F><<<(tiles + per_cta - 1) / per_cta, kThreads, 0, s>>>(a, p, tiles);
     return cudaGetLastError();
 }
 
