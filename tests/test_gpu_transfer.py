@@ -108,3 +108,29 @@ def test_decode_checks_its_arguments():
         sz.splitzip_decode_from_host(bad, nbytes, torch.empty_like(x), scratch, streams)
     with pytest.raises(sz.SplitZipError):
         sz.splitzip_decode_from_host(payload, nbytes, torch.empty_like(x), scratch[:1024], streams)
+
+
+def test_encode_checks_its_arguments():
+    """Rejected on the host before any work is enqueued."""
+    ensure_library()
+    fmt, chunk, se = "bf16", 1024, 1 << 16
+    x = _kv(fmt, 100000, seed=7)
+    cb = [int(c) for c in oracle.calibrate(host_bits(x), fmt)[0]]
+    scratch, streams = sz.alloc_transfer_scratch(se, chunk, fmt), _streams()
+    payload = torch.empty(sz.splitzip_payload_bytes_bound(x.numel(), chunk, se, x.numel(), fmt),
+                          dtype=torch.uint8).pin_memory()
+    bad_calls = [
+        dict(slice_elems=se + 8),                        # not a multiple of the chunk size
+        dict(slice_elems=512),                           # smaller than a chunk
+        dict(codebooks=[cb, cb, cb]),                    # two slices: neither one codebook nor one each
+        dict(codebooks=[cb[0]] * 16),                    # repeated exponents
+        dict(streams=[streams[0], streams[0], streams[2]]),  # streams must differ
+        dict(scratch=scratch[: scratch.numel() // 2]),  # scratch too small
+    ]
+    for bad in bad_calls:
+        kw = dict(slice_elems=se, codebooks=cb, streams=streams, scratch=scratch)
+        kw.update(bad)
+        with pytest.raises(sz.SplitZipError) as err:
+            sz.splitzip_encode_to_host(x, chunk, kw["codebooks"], kw["slice_elems"], payload,
+                                       kw["scratch"], kw["streams"], fmt)
+        assert err.value.status == sz.ERR_INVALID_ARG, bad
