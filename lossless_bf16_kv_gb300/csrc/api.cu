@@ -9,6 +9,7 @@
 #include "../../include/splitzip.h"
 #include "../../include/splitzip_testing.h"
 #include "kernels.h"
+#include "trace.h"
 
 using namespace splitzip;
 
@@ -204,18 +205,21 @@ uint64_t splitzip_compressed_bytes_e5m2(uint64_t n, uint32_t chunk_size, uint64_
 
 splitzip_status splitzip_calibrate(const void* d_x, uint64_t n, splitzip_codebook* cb_out,
                                    double* coverage_out, void* d_workspace, splitzip_stream_t s) {
+    TraceRange trace("splitzip_calibrate");
     return calibrate_sync_impl(d_x, n, cb_out, coverage_out, d_workspace, (cudaStream_t)s, false);
 }
 
 splitzip_status splitzip_calibrate_e5m2(const void* d_x, uint64_t n, splitzip_codebook* cb_out,
                                         double* coverage_out, void* d_workspace,
                                         splitzip_stream_t s) {
+    TraceRange trace("splitzip_calibrate_e5m2");
     return calibrate_sync_impl(d_x, n, cb_out, coverage_out, d_workspace, (cudaStream_t)s, true);
 }
 
 splitzip_status splitzip_calibrate_async(const void* d_x, uint64_t n, uint8_t* d_cb_out,
                                          uint64_t* d_covered_out, void* d_workspace,
                                          splitzip_stream_t s) {
+    TraceRange trace("splitzip_calibrate_async");
     return calibrate_async_impl(d_x, n, d_cb_out, d_covered_out, d_workspace, (cudaStream_t)s,
                                 false);
 }
@@ -223,29 +227,34 @@ splitzip_status splitzip_calibrate_async(const void* d_x, uint64_t n, uint8_t* d
 splitzip_status splitzip_calibrate_async_e5m2(const void* d_x, uint64_t n, uint8_t* d_cb_out,
                                               uint64_t* d_covered_out, void* d_workspace,
                                               splitzip_stream_t s) {
+    TraceRange trace("splitzip_calibrate_async_e5m2");
     return calibrate_async_impl(d_x, n, d_cb_out, d_covered_out, d_workspace, (cudaStream_t)s,
                                 true);
 }
 
 splitzip_status splitzip_histogram(const void* d_x, uint64_t n, uint64_t* d_hist_out,
                                    void* d_workspace, splitzip_stream_t s) {
+    TraceRange trace("splitzip_histogram");
     return histogram_impl(d_x, n, d_hist_out, d_workspace, (cudaStream_t)s, false);
 }
 
 splitzip_status splitzip_histogram_e5m2(const void* d_x, uint64_t n, uint64_t* d_hist_out,
                                         void* d_workspace, splitzip_stream_t s) {
+    TraceRange trace("splitzip_histogram_e5m2");
     return histogram_impl(d_x, n, d_hist_out, d_workspace, (cudaStream_t)s, true);
 }
 
 splitzip_status splitzip_encode(const void* d_x, uint64_t n, uint32_t chunk_size,
                                 const splitzip_codebook* cb, const splitzip_streams* out,
                                 void* d_workspace, splitzip_stream_t s) {
+    TraceRange trace("splitzip_encode");
     return encode_impl(d_x, n, chunk_size, cb, out, d_workspace, (cudaStream_t)s, false, 0, 0);
 }
 
 splitzip_status splitzip_encode_e5m2(const void* d_x, uint64_t n, uint32_t chunk_size,
                                      const splitzip_codebook* cb, const splitzip_streams* out,
                                      void* d_workspace, splitzip_stream_t s) {
+    TraceRange trace("splitzip_encode_e5m2");
     return encode_impl(d_x, n, chunk_size, cb, out, d_workspace, (cudaStream_t)s, true, 0, 0);
 }
 
@@ -262,6 +271,7 @@ splitzip_status splitzip_encode_test(const void* d_x, uint64_t n, uint32_t chunk
 
 splitzip_status splitzip_encode_status(const void* d_workspace, splitzip_stream_t s,
                                        uint64_t* n_escapes_out) {
+    TraceRange trace("splitzip_encode_status");
     if (!d_workspace || !aligned(d_workspace, 16)) return SPLITZIP_ERR_INVALID_ARG;
     const WsHeader* hdr = static_cast<const WsHeader*>(d_workspace);
     struct {
@@ -284,12 +294,14 @@ splitzip_status splitzip_encode_status(const void* d_workspace, splitzip_stream_
 
 splitzip_status splitzip_decode(const splitzip_streams* in, uint64_t n, uint32_t chunk_size,
                                 const splitzip_codebook* cb, void* d_y, splitzip_stream_t s) {
+    TraceRange trace("splitzip_decode");
     return decode_impl(in, n, chunk_size, cb, d_y, (cudaStream_t)s, false);
 }
 
 splitzip_status splitzip_decode_e5m2(const splitzip_streams* in, uint64_t n,
                                      uint32_t chunk_size, const splitzip_codebook* cb, void* d_y,
                                      splitzip_stream_t s) {
+    TraceRange trace("splitzip_decode_e5m2");
     return decode_impl(in, n, chunk_size, cb, d_y, (cudaStream_t)s, true);
 }
 

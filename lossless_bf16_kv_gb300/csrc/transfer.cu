@@ -19,6 +19,7 @@
 #include "../../include/splitzip.h"
 #include "../../include/splitzip_transfer.h"
 #include "common.cuh"
+#include "trace.h"
 
 namespace {
 
@@ -278,6 +279,7 @@ splitzip_status splitzip_encode_to_host(const void* x, uint64_t n, uint32_t form
                                         uint64_t* payload_bytes, void* d_scratch,
                                         size_t scratch_bytes, splitzip_stream_t s_compute,
                                         splitzip_stream_t s_h2d, splitzip_stream_t s_d2h) {
+    splitzip::TraceRange trace("splitzip_encode_to_host");
     if (!x || !cbs || !h_payload || !payload_bytes || !d_scratch) return SPLITZIP_ERR_INVALID_ARG;
     if (!format_ok(format) || !chunk_ok(chunk_size) || n == 0 || n > SPLITZIP_MAX_ELEMENTS)
         return SPLITZIP_ERR_INVALID_ARG;
@@ -434,6 +436,7 @@ splitzip_status splitzip_decode_from_host(const void* h_payload, uint64_t bytes,
                                           uint64_t n, void* d_scratch, size_t scratch_bytes,
                                           splitzip_stream_t s_compute, splitzip_stream_t s_h2d,
                                           splitzip_stream_t s_d2h) {
+    splitzip::TraceRange trace("splitzip_decode_from_host");
     if (!h_payload || !y || !d_scratch) return SPLITZIP_ERR_INVALID_ARG;
     splitzip_payload_info info;
     if (splitzip_payload_parse(h_payload, bytes, &info, nullptr, 0) != SPLITZIP_OK)
