@@ -296,6 +296,8 @@ splitzip_status splitzip_encode_to_host(const void* x, uint64_t n, uint32_t form
     bool ok = false;
     const bool host_in = is_host_pointer(x, &ok);
     if (!ok) return SPLITZIP_ERR_INVALID_ARG;
+    // The host writes the payload's header, table and padding itself.
+    if (!is_host_pointer(h_payload, &ok) || !ok) return SPLITZIP_ERR_INVALID_ARG;
 
     const cudaStream_t sc = (cudaStream_t)s_compute, sh = (cudaStream_t)s_h2d,
                        sd = (cudaStream_t)s_d2h;
@@ -438,6 +440,8 @@ splitzip_status splitzip_decode_from_host(const void* h_payload, uint64_t bytes,
                                           splitzip_stream_t s_d2h) {
     splitzip::TraceRange trace("splitzip_decode_from_host");
     if (!h_payload || !y || !d_scratch) return SPLITZIP_ERR_INVALID_ARG;
+    bool queried = false;  // the host parses the payload: it must be host memory
+    if (!is_host_pointer(h_payload, &queried) || !queried) return SPLITZIP_ERR_INVALID_ARG;
     splitzip_payload_info info;
     if (splitzip_payload_parse(h_payload, bytes, &info, nullptr, 0) != SPLITZIP_OK)
         return SPLITZIP_ERR_INVALID_ARG;

@@ -134,3 +134,19 @@ def test_encode_checks_its_arguments():
             sz.splitzip_encode_to_host(x, chunk, kw["codebooks"], kw["slice_elems"], payload,
                                        kw["scratch"], kw["streams"], fmt)
         assert err.value.status == sz.ERR_INVALID_ARG, bad
+
+
+def test_payload_must_be_host_memory():
+    ensure_library()
+    fmt, chunk, se = "bf16", 1024, 1 << 16
+    x = _kv(fmt, 100000, seed=8)
+    cb = [int(c) for c in oracle.calibrate(host_bits(x), fmt)[0]]
+    scratch, streams = sz.alloc_transfer_scratch(se, chunk, fmt), _streams()
+    payload, nbytes = sz.encode_to_host(x, chunk, cb, se, scratch, streams, fmt)
+    on_device = payload.cuda()
+    with pytest.raises(sz.SplitZipError) as err:
+        sz.splitzip_encode_to_host(x, chunk, cb, se, on_device, scratch, streams, fmt)
+    assert err.value.status == sz.ERR_INVALID_ARG
+    with pytest.raises(sz.SplitZipError) as err:
+        sz.splitzip_decode_from_host(on_device, nbytes, torch.empty_like(x), scratch, streams)
+    assert err.value.status == sz.ERR_INVALID_ARG
