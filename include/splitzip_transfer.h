@@ -118,8 +118,9 @@ size_t splitzip_transfer_scratch_bytes(uint32_t format, uint64_t slice_elems,
                                        uint32_t chunk_size);
 
 /* Encode the n elements at x slice by slice into the host payload h_payload
- * (capacity payload_capacity bytes), writing the whole payload including its
- * header; *payload_bytes receives its size.
+ * (capacity payload_capacity bytes; host memory, else SPLITZIP_ERR_INVALID_ARG),
+ * writing the whole payload including its header; *payload_bytes receives its
+ * size.
  *
  * x: device memory, or host memory (pinned for speed), 16-byte aligned; the
  *    call finds out which with cudaPointerGetAttributes and, for host input,
@@ -148,8 +149,8 @@ splitzip_status splitzip_encode_to_host(const void* x, uint64_t n, uint32_t form
                                         size_t scratch_bytes, splitzip_stream_t s_compute,
                                         splitzip_stream_t s_h2d, splitzip_stream_t s_d2h);
 
-/* Decode a host payload (as written by splitzip_encode_to_host, `bytes` long)
- * into y: n elements of the payload's format, in device memory or in host
+/* Decode a host payload (as written by splitzip_encode_to_host, `bytes` long,
+ * in host memory, else SPLITZIP_ERR_INVALID_ARG) into y: n elements of the payload's format, in device memory or in host
  * memory (pinned for speed), 16-byte aligned.  The payload is validated with
  * splitzip_payload_parse first; n must equal its element count.  Slices are
  * copied to the device, decoded and (for host output) copied back, the three
