@@ -66,18 +66,20 @@ __device__ __forceinline__ uint32_t assemble_e5m2(uint32_t f12, uint32_t ex) {
 // (any result in [b, e] otherwise).  All 32 lanes of a warp call it.
 __device__ uint32_t lower_bound_warp(const uint16_t* pos, uint32_t b, uint32_t e, uint32_t r) {
     const uint32_t lane = threadIdx.x & 31;
+    // b <= e throughout; probe indices are formed in 64 bits so that e near
+    // 2^32 cannot wrap them.
     while (e - b > 32) {
         const uint32_t step = (e - b + 31) / 32;
-        const uint32_t j = b + lane * step;
+        const uint64_t j = (uint64_t)b + (uint64_t)lane * step;
         const bool lt = j < e && pos[j] < r;
         const uint32_t k = __popc(__ballot_sync(0xFFFFFFFFu, lt));
         if (k == 0) return b;
-        const uint32_t nb = b + (k - 1) * step + 1;
-        const uint32_t ne = min(e, b + k * step);
+        const uint32_t nb = b + (k - 1) * step + 1;  // <= e: lane k - 1 probed below e
+        const uint64_t ne = (uint64_t)b + (uint64_t)k * step;
         b = nb;
-        e = ne;
+        e = ne < e ? (uint32_t)ne : e;
     }
-    const bool lt = b + lane < e && pos[b + lane] < r;
+    const bool lt = lane < e - b && pos[b + lane] < r;
     return b + __popc(__ballot_sync(0xFFFFFFFFu, lt));
 }
 
@@ -117,9 +119,9 @@ struct EscBatch {
 };
 
 __device__ __forceinline__ EscBatch load_batch(const DecodeArgs& a, uint32_t b, uint32_t hi) {
-    const uint32_t j = b + (threadIdx.x & 31);
+    const uint32_t lane = threadIdx.x & 31, j = b + lane;
     EscBatch e{0xFFFFFFFFu, 0u, 0u};
-    if (j < hi) {
+    if (b < hi && lane < hi - b) {  // not j < hi: b + lane may wrap
         e.j = j;
         e.pos = a.esc_pos[j];
         e.val = a.esc_val[j];
@@ -161,7 +163,10 @@ __device__ __forceinline__ void patch_escapes(const DecodeArgs& a, const EscBatc
         }
     };
     put(eb);
-    for (uint32_t b = lo + 32; b < hi; b += 32) put(load_batch(a, b, hi));
+    for (uint32_t b = lo; hi - b > 32;) {  // lo <= b < hi; no sum that could wrap
+        b += 32;
+        put(load_batch(a, b, hi));
+    }
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < F::kExWords; q++) ex.e[q] = pex[q * 32 + lane];
@@ -197,7 +202,7 @@ __device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* sm
     constexpr uint32_t kPieces = F::kStageBytes / 16;
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t warps = gridDim.x * kWarps;
-    const uint32_t nseg = (a.n + F::kSeg - 1) / F::kSeg;
+    const uint32_t nseg = (uint32_t)(((uint64_t)a.n + F::kSeg - 1) / F::kSeg);  // n may be 2^32 - 1
     const uint32_t full_segs = a.n / (uint32_t)F::kSeg;
     const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
     uint8_t* ring = smem + (size_t)warp * F::kStageBytes;  // stage s at ring + s * kWarps * kStageBytes
@@ -283,7 +288,7 @@ template <class F>
 __device__ __forceinline__ void decode_segments_regs(const DecodeArgs& a, uint8_t* smem) {
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t warps = gridDim.x * kWarps;
-    const uint32_t nseg = (a.n + F::kSeg - 1) / F::kSeg;
+    const uint32_t nseg = (uint32_t)(((uint64_t)a.n + F::kSeg - 1) / F::kSeg);  // n may be 2^32 - 1
     const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
     uint32_t* pex = reinterpret_cast<uint32_t*>(smem) + (size_t)warp * F::kExWords * 32;
     uint32_t seg = blockIdx.x * kWarps + warp;
@@ -353,7 +358,7 @@ struct Bf16Seg {
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
             const uint32_t i = s0 + 256 * k + 8 * lane;
-            if (full || i + 8 <= s1) {
+            if (full || (uint64_t)i + 8 <= s1) {
                 d.code[k] = ld_stream4(a.codes + i / 2);
                 d.sm[k] = ld_stream8(a.signman + i);
             } else {
@@ -394,7 +399,7 @@ struct Bf16Seg {
             if (!full && i >= s1) continue;
             const uint2 o0 = assemble_bf16(d.sm[k].x, ex.e[2 * k]);
             const uint2 o1 = assemble_bf16(d.sm[k].y, ex.e[2 * k + 1]);
-            if (full || i + 8 <= s1) {
+            if (full || s1 - i >= 8) {  // i < s1 here
                 st_stream16(a.y + 2ull * i, make_uint4(o0.x, o0.y, o1.x, o1.y));
             } else {
                 const uint32_t w[4] = {o0.x, o0.y, o1.x, o1.y};
@@ -449,7 +454,7 @@ struct E5m2Seg {
         for (int k = 0; k < kGroups; k++) {
             const uint32_t i = s0 + 1024 * k + 32 * lane;
             const uint8_t* smp = a.signman + (uint64_t)(i / 32) * 12;
-            if (full || i + 32 <= s1) {
+            if (full || (uint64_t)i + 32 <= s1) {
                 d.code[k] = ld_stream16(a.codes + i / 2);
                 d.smw[k][0] = ld_stream4(smp);
                 d.smw[k][1] = ld_stream4(smp + 4);
@@ -503,7 +508,7 @@ struct E5m2Seg {
                 uint8_t* yb = a.y + (s0 + 32 * lane) + 1024 * k;
                 st_stream16(yb, make_uint4(out[0], out[1], out[2], out[3]));
                 st_stream16(yb + 16, make_uint4(out[4], out[5], out[6], out[7]));
-            } else if (i + 32 <= s1) {
+            } else if (s1 - i >= 32) {  // i < s1 here
                 st_stream16(a.y + i, make_uint4(out[0], out[1], out[2], out[3]));
                 st_stream16(a.y + i + 16, make_uint4(out[4], out[5], out[6], out[7]));
             } else {

@@ -223,7 +223,7 @@ struct Bf16Tile {
             kp.ent[k][0] = kp.ent[k][1] = 0;
             if (i >= a.n) continue;
             uint4 v;
-            const bool whole = i + 8 <= a.n;
+            const bool whole = a.n - i >= 8;  // i < n here
             if (whole) {
                 v = *reinterpret_cast<const uint4*>(stage + 2 * l);
             } else {
@@ -313,7 +313,7 @@ struct E5m2Tile {
 #pragma unroll
         for (int m = 0; m < 8; m++) kp.ent[m] = 0;
         if (!full && i >= a.n) return;
-        const bool whole = full || i + 32 <= a.n;
+        const bool whole = full || a.n - i >= 32;  // i < n when not full
         uint32_t w[8];
         if (whole) {
             const uint4 v0 = *reinterpret_cast<const uint4*>(stage + l);

@@ -348,7 +348,7 @@ struct E5m2Dense {
 #pragma unroll
         for (int m = 0; m < 8; m++) kp.ent[m] = 0;
         if (i >= a.n) return;
-        const bool whole = i + 32 <= a.n;
+        const bool whole = a.n - i >= 32;  // i < n here
         uint32_t w[8];
         if (whole) {
             const uint4 v0 = ld_stream16(a.x + i);
