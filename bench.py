@@ -538,6 +538,8 @@ def main():
     dominant = "encode" if enc >= dec else "decode"
     kernel = KERNELS[dominant][0 if res["fmt"] == "bf16" else 1]
     dom_ms = max(enc, dec)
+    other_kernel = KERNELS["decode" if dominant == "encode" else "encode"][
+        0 if res["fmt"] == "bf16" else 1]
     achieved = algo / (dom_ms / 1e3) / 1e9
     from lossless_bf16_kv_gb300 import splitzip as sz
     comp = sz.splitzip_compressed_bytes(n, res["chunk"], E, res["fmt"])
@@ -563,8 +565,8 @@ def main():
         "roofline_other": {"op": "decode" if dominant == "encode" else "encode",
                            "achieved": round(algo / (min(enc, dec) / 1e3) / 1e9, 1),
                            "frac": round(algo / (min(enc, dec) / 1e3) / 1e9 / peak, 4),
-                           "kernel": KERNELS["decode" if dominant == "encode" else "encode"][
-                               0 if res["fmt"] == "bf16" else 1]},
+                           "kernel": other_kernel,
+                           "traffic": stored_traffic(other_kernel, w.name)},
         "gpu_launches": 4 * K,  # encode: dense, prefix, place; decode: one
         "clocks": res["clocks"],
         "context": {"pages_h200_encode_gbs": 613.3, "pages_h200_decode_gbs": 2181.8,
