@@ -107,8 +107,12 @@ struct Bf16Dense {
     struct Tables {
         uint32_t t[4][256];
     };
+    // Escape exponents are read again from the tile's input (the ring stage,
+    // still intact during the bookkeeping, or global memory for the partial
+    // tile), so no input words stay live in registers.
+    static constexpr bool kEmitFromInput = true;
+    static constexpr int kMinBlocks = 6;  // resident CTAs per SM (shared memory allows 6)
     struct Keep {
-        uint4 v[kGroups];       // the input words (escape exponents are re-read from them)
         uint32_t miss[kGroups]; // escape flags: bits 0..3 elements 0..3, bits 16..19 elements 4..7
         uint32_t cnt;           // escapes of group k in byte k (at most 8 each)
     };
@@ -191,7 +195,6 @@ struct Bf16Dense {
             uint32_t codes, miss;
             uint2 sm;
             group(tb, v[k], codes, sm, miss);
-            kp.v[k] = v[k];
             kp.miss[k] = miss;
             st_stream4(cbase + k * (kThreads * 4), codes);
             st_stream8(sbase + k * (kThreads * 8), sm);
@@ -210,7 +213,6 @@ struct Bf16Dense {
         for (int k = 0; k < kGroups; k++) {
             const uint32_t i = t0 + loff(k);
             kp.miss[k] = 0;
-            kp.v[k] = make_uint4(0, 0, 0, 0);
             if (i >= a.n) continue;
             const uint32_t rem = a.n - i;
             const bool whole = rem >= 8;
@@ -228,7 +230,6 @@ struct Bf16Dense {
             uint32_t codes, miss;
             uint2 sm;
             group(tb, v, codes, sm, miss);
-            kp.v[k] = v;
             kp.miss[k] = miss;
             kp.cnt |= (uint32_t)__popc(miss) << (8 * k);
             if (whole) {
@@ -251,7 +252,7 @@ struct Bf16Dense {
     // number of lower lanes whose same group has an escape, a segment's total
     // the population of that ballot.
     static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
-                                                           uint16_t* ent) {
+                                                           uint16_t* ent, const uint16_t* in) {
         const uint32_t lane = threadIdx.x & 31, lt = (1u << lane) - 1u;
         uint32_t has[kGroups];
 #pragma unroll
@@ -263,13 +264,17 @@ struct Bf16Dense {
             uint32_t excl = 0;
 #pragma unroll
             for (int k = 0; k < kGroups; k++) excl |= (uint32_t)__popc(has[k] & lt) << (8 * k);
-            emit(kp, excl, ent);
+            emit(kp, excl, ent, in);
         }
     }
 
     // The first kSegCap escapes of each segment into its workspace entries.
     // excl: the exclusive escape ranks of this lane's groups, one per byte.
-    static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent) {
+    // in: the tile's input, element-indexed (group k of this thread at
+    // loff(k)): the ring stage of a full tile, global memory for the partial
+    // one (whose escapes all lie below n).
+    static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent,
+                                                const uint16_t* in) {
         const uint32_t lane = threadIdx.x & 31;
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
@@ -277,14 +282,12 @@ struct Bf16Dense {
             if (!m) continue;
             uint32_t g = (excl >> (8 * k)) & 0xFFu;
             uint16_t* e = ent + slot(k) * kSegCap;
-            const uint32_t w[4] = {kp.v[k].x, kp.v[k].y, kp.v[k].z, kp.v[k].w};
+            const uint16_t* x = in + loff(k);
             while (m && g < (uint32_t)kSegCap) {
                 const uint32_t b = __ffs(m) - 1;  // bit b: element (b & 3) + 4 * (b >> 4)
                 m &= m - 1;
                 const uint32_t j = (b & 3u) + ((b >> 4) << 2);
-                const uint32_t word = j >> 1;
-                const uint32_t wv = word == 0 ? w[0] : word == 1 ? w[1] : word == 2 ? w[2] : w[3];
-                const uint32_t ex = (wv >> (7 + 16 * (j & 1))) & kExpMask;
+                const uint32_t ex = ((uint32_t)x[j] >> 7) & kExpMask;
                 e[g++] = (uint16_t)((8 * lane + j) | (ex << kOffBits));
             }
         }
@@ -306,14 +309,38 @@ struct E5m2Dense {
     static constexpr int kSegCap = kEntries / kSegs;  // 32
     static constexpr int kOffBits = 10;
     static constexpr uint32_t kExpMask = 0x1Fu;
+    // Code table indexed by the raw byte with its sign bit cleared (exponent
+    // in bits 2..6, mantissa in bits 0..1): entry = code, or kMissEntry for an
+    // exponent outside the codebook.  The four bytes of one exponent share a
+    // word, so lanes with different exponents always read different banks.
     struct Tables {
-        uint8_t t[256];
+        uint8_t t[128];
     };
+    static constexpr bool kEmitFromInput = false;  // the input words stay in Keep
+    static constexpr int kMinBlocks = 6;  // resident CTAs per SM (registers cap it at 40 each)
     struct Keep {
-        uint32_t ex[8], ent[8], cnt;
+        uint32_t w[8], ent[8], cnt;
     };
     static __device__ __forceinline__ void build_tables(Tables& tb, const uint32_t (&cbw)[4]) {
-        build_table(tb.t, cbw);
+        const uint32_t tid = threadIdx.x;
+        if (tid < 128) {
+            const uint32_t e = tid >> 2;
+            uint32_t ent = kMissEntry;
+#pragma unroll
+            for (int k = 0; k < 16; k++)  // codebook entries are distinct
+                if (((cbw[k >> 2] >> (8 * (k & 3))) & 0xFFu) == e) ent = (uint32_t)k;
+            tb.t[tid] = (uint8_t)ent;
+        }
+        __syncthreads();
+    }
+    // Entries of the four bytes of w, one per byte.
+    static __device__ __forceinline__ uint32_t lookup_raw4(const uint8_t* t, uint32_t w) {
+        const uint32_t m = w & 0x7F7F7F7Fu;
+        const uint32_t e0 = t[__byte_perm(m, 0u, 0x4440)];
+        const uint32_t e1 = t[__byte_perm(m, 0u, 0x4441)];
+        const uint32_t e2 = t[__byte_perm(m, 0u, 0x4442)];
+        const uint32_t e3 = t[__byte_perm(m, 0u, 0x4443)];
+        return __byte_perm(__byte_perm(e0, e1, 0x0040), __byte_perm(e2, e3, 0x0040), 0x5410);
     }
     static __device__ __forceinline__ uint32_t slot(int) { return threadIdx.x >> 5; }
     static __device__ __forceinline__ uint32_t storage(uint32_t s) { return s; }
@@ -379,9 +406,12 @@ struct E5m2Dense {
         kp.cnt = 0;
         uint32_t f12[8];
 #pragma unroll
-        for (int m = 0; m < 8; m++) split_e5m2(w[m], kp.ex[m], f12[m]);
+        for (int m = 0; m < 8; m++) {
+            f12[m] = fields12_e5m2(w[m]);
+            kp.w[m] = w[m];
+        }
 #pragma unroll
-        for (int m = 0; m < 8; m++) kp.ent[m] = lookup4(table, kp.ex[m]);
+        for (int m = 0; m < 8; m++) kp.ent[m] = lookup_raw4(table, w[m]);
         uint4 codes;
         codes.x = pack_nibbles(kp.ent[0], kp.ent[1]);
         codes.y = pack_nibbles(kp.ent[2], kp.ent[3]);
@@ -413,14 +443,15 @@ struct E5m2Dense {
     static __device__ __forceinline__ bool multi(const Keep& kp) { return kp.cnt >= 2; }
     // Counts and escapes when no lane of the warp holds more than one escape.
     static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
-                                                           uint16_t* ent) {
+                                                           uint16_t* ent, const uint16_t*) {
         const uint32_t lane = threadIdx.x & 31;
         const uint32_t has = __ballot_sync(0xFFFFFFFFu, kp.cnt != 0);
         if (lane == 0) row[slot(0)] = (uint16_t)__popc(has);
-        if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent);
+        if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent, nullptr);
     }
 
-    static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent) {
+    static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent,
+                                                const uint16_t*) {
         if (!kp.cnt) return;
         const uint32_t lane = threadIdx.x & 31;
         uint32_t g = excl;
@@ -432,7 +463,7 @@ struct E5m2Dense {
             for (int b = 0; b < 4; b++) {
                 if ((kp.ent[m] >> (8 * b)) & kMissEntry) {
                     if (g < (uint32_t)kSegCap)
-                        e[g] = (uint16_t)((32 * lane + 4 * m + b) | (((kp.ex[m] >> (8 * b)) & kExpMask) << kOffBits));
+                        e[g] = (uint16_t)((32 * lane + 4 * m + b) | (((kp.w[m] >> (8 * b + 2)) & kExpMask) << kOffBits));
                     g++;
                 }
             }
@@ -462,7 +493,8 @@ constexpr size_t dense_smem_bytes() {
 }
 
 template <class F>
-__global__ void __launch_bounds__(kThreads) dense_kernel(const EncodeArgs a, const MultiPtrs p) {
+__global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const EncodeArgs a,
+                                                                       const MultiPtrs p) {
     constexpr int L = F::kLoads, S = kDenseStages;
     extern __shared__ uint4 ring[];  // [S][L][kThreads]
     __shared__ typename F::Tables tables;
@@ -484,26 +516,37 @@ __global__ void __launch_bounds__(kThreads) dense_kernel(const EncodeArgs a, con
     for (uint32_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
         const uint32_t t0 = tile * (uint32_t)kTileElems;
         typename F::Keep kp;
+        const uint16_t* in;  // the tile's input, for formats that read escapes from it
         if (tile < full_tiles) {
             cp_async_wait<S - 1>();  // this tile's group (the oldest pending) has landed
             if (F::kSharedStage) __syncwarp();  // the warp's copies, visible to all its lanes
             F::compute_full(a, tables, t0, ring + slot * L * kThreads, kp);
+            in = reinterpret_cast<const uint16_t*>(ring + slot * L * kThreads);
         } else {
             F::process_partial(a, tables, t0, kp);
+            in = reinterpret_cast<const uint16_t*>(a.x) + t0;
         }
-        if (F::kSharedStage) __syncwarp();  // every lane has read the stage before the refill
-        fill(tile + S * gridDim.x, slot);
-        slot = slot + 1 == S ? 0 : slot + 1;
+        // A format that reads its escapes from the stage refills it after the
+        // bookkeeping; the others refill it first.
+        if (!F::kEmitFromInput) {
+            if (F::kSharedStage) __syncwarp();  // every lane has read the stage before the refill
+            fill(tile + S * gridDim.x, slot);
+        }
         uint16_t* row = p.seg_cnt + (size_t)tile * kSegsMax;
         uint16_t* ent = p.seg_ent + (size_t)tile * kEntries;
         if (!__any_sync(0xFFFFFFFFu, F::multi(kp))) {
-            F::bookkeep_single(kp, row, ent);
+            F::bookkeep_single(kp, row, ent, in);
         } else {
             uint32_t excl, e31, p31;
             warp_scan_excl(kp.cnt, excl, e31, p31);
             if (lane == 0) F::store_counts(row, e31, p31);
-            if (kp.cnt) F::emit(kp, excl, ent);
+            if (kp.cnt) F::emit(kp, excl, ent, in);
         }
+        if (F::kEmitFromInput) {
+            if (F::kSharedStage) __syncwarp();
+            fill(tile + S * gridDim.x, slot);
+        }
+        slot = slot + 1 == S ? 0 : slot + 1;
     }
     cp_async_wait<0>();
 }

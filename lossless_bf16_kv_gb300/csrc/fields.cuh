@@ -55,4 +55,11 @@ __device__ __forceinline__ void split_e5m2(uint32_t w, uint32_t& ex, uint32_t& f
     f12 = (t & 0x3Fu) | ((t >> 10) & 0xFC0u);
 }
 
+// The four three-bit fields of 4 E5M2 bytes alone, packed as by split_e5m2.
+__device__ __forceinline__ uint32_t fields12_e5m2(uint32_t w) {
+    const uint32_t f = ((w >> 5) & 0x04040404u) | (w & 0x03030303u);
+    const uint32_t t = f | (f >> 5);
+    return (t & 0x3Fu) | ((t >> 10) & 0xFC0u);
+}
+
 }  // namespace splitzip
