@@ -107,10 +107,7 @@ struct Bf16Dense {
     struct Tables {
         uint32_t t[4][256];
     };
-    // Escape exponents are read again from the tile's input (the ring stage,
-    // still intact during the bookkeeping, or global memory for the partial
-    // tile), so no input words stay live in registers.
-    static constexpr bool kEmitFromInput = true;
+    static constexpr int kElemBytes = 2;
     static constexpr int kMinBlocks = 6;  // resident CTAs per SM (shared memory allows 6)
     struct Keep {
         uint32_t miss[kGroups]; // escape flags: bits 0..3 elements 0..3, bits 16..19 elements 4..7
@@ -252,7 +249,7 @@ struct Bf16Dense {
     // number of lower lanes whose same group has an escape, a segment's total
     // the population of that ballot.
     static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
-                                                           uint16_t* ent, const uint16_t* in) {
+                                                           uint16_t* ent, const uint8_t* in) {
         const uint32_t lane = threadIdx.x & 31, lt = (1u << lane) - 1u;
         uint32_t has[kGroups];
 #pragma unroll
@@ -270,11 +267,9 @@ struct Bf16Dense {
 
     // The first kSegCap escapes of each segment into its workspace entries.
     // excl: the exclusive escape ranks of this lane's groups, one per byte.
-    // in: the tile's input, element-indexed (group k of this thread at
-    // loff(k)): the ring stage of a full tile, global memory for the partial
-    // one (whose escapes all lie below n).
+    // in: the tile's input (group k of this thread at element loff(k)).
     static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent,
-                                                const uint16_t* in) {
+                                                const uint8_t* in) {
         const uint32_t lane = threadIdx.x & 31;
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
@@ -282,7 +277,7 @@ struct Bf16Dense {
             if (!m) continue;
             uint32_t g = (excl >> (8 * k)) & 0xFFu;
             uint16_t* e = ent + slot(k) * kSegCap;
-            const uint16_t* x = in + loff(k);
+            const uint16_t* x = reinterpret_cast<const uint16_t*>(in) + loff(k);
             while (m && g < (uint32_t)kSegCap) {
                 const uint32_t b = __ffs(m) - 1;  // bit b: element (b & 3) + 4 * (b >> 4)
                 m &= m - 1;
@@ -316,10 +311,11 @@ struct E5m2Dense {
     struct Tables {
         uint8_t t[128];
     };
-    static constexpr bool kEmitFromInput = false;  // the input words stay in Keep
+    static constexpr int kElemBytes = 1;
     static constexpr int kMinBlocks = 6;  // resident CTAs per SM (registers cap it at 40 each)
     struct Keep {
-        uint32_t w[8], ent[8], cnt;
+        uint32_t mm;   // escape flags of the lane's 32 elements, bit j for element j
+        uint32_t cnt;  // popcount of mm
     };
     static __device__ __forceinline__ void build_tables(Tables& tb, const uint32_t (&cbw)[4]) {
         const uint32_t tid = threadIdx.x;
@@ -372,8 +368,7 @@ struct E5m2Dense {
                                                            uint32_t t0, Keep& kp) {
         const uint32_t i = t0 + threadIdx.x * 32;
         kp.cnt = 0;
-#pragma unroll
-        for (int m = 0; m < 8; m++) kp.ent[m] = 0;
+        kp.mm = 0;
         if (i >= a.n) return;
         const bool whole = a.n - i >= 32;  // i < n here
         uint32_t w[8];
@@ -403,22 +398,26 @@ struct E5m2Dense {
     static __device__ __forceinline__ void finish(const EncodeArgs& a, const uint8_t* table,
                                                   uint32_t i, const uint32_t (&w)[8], bool whole,
                                                   Keep& kp) {
-        kp.cnt = 0;
-        uint32_t f12[8];
+        uint32_t f12[8], ent[8];
+#pragma unroll
+        for (int m = 0; m < 8; m++) f12[m] = fields12_e5m2(w[m]);
+#pragma unroll
+        for (int m = 0; m < 8; m++) ent[m] = lookup_raw4(table, w[m]);
+        uint4 codes;
+        codes.x = pack_nibbles(ent[0], ent[1]);
+        codes.y = pack_nibbles(ent[2], ent[3]);
+        codes.z = pack_nibbles(ent[4], ent[5]);
+        codes.w = pack_nibbles(ent[6], ent[7]);
+        // Escape flags (bit 4 of each entry byte, at bits 4, 12, 20, 28) to
+        // bits 4m..4m+3: multiplying by 2^0 + 2^7 + 2^14 + 2^21 moves flag b
+        // to bit 25 + b; every other partial product lands below bit 25.
+        kp.mm = 0;
 #pragma unroll
         for (int m = 0; m < 8; m++) {
-            f12[m] = fields12_e5m2(w[m]);
-            kp.w[m] = w[m];
+            const uint32_t nib = ((ent[m] & 0x10101010u) * 0x00204081u) >> 25;
+            kp.mm |= nib << (4 * m);
         }
-#pragma unroll
-        for (int m = 0; m < 8; m++) kp.ent[m] = lookup_raw4(table, w[m]);
-        uint4 codes;
-        codes.x = pack_nibbles(kp.ent[0], kp.ent[1]);
-        codes.y = pack_nibbles(kp.ent[2], kp.ent[3]);
-        codes.z = pack_nibbles(kp.ent[4], kp.ent[5]);
-        codes.w = pack_nibbles(kp.ent[6], kp.ent[7]);
-#pragma unroll
-        for (int m = 0; m < 8; m += 2) kp.cnt += miss_count(kp.ent[m], kp.ent[m + 1]);
+        kp.cnt = __popc(kp.mm);
         // 8 x 12 bits -> 96 bits, little-endian.
         const uint32_t s0 = f12[0] | (f12[1] << 12) | (f12[2] << 24);
         const uint32_t s1 = (f12[2] >> 8) | (f12[3] << 4) | (f12[4] << 16) | (f12[5] << 28);
@@ -443,30 +442,24 @@ struct E5m2Dense {
     static __device__ __forceinline__ bool multi(const Keep& kp) { return kp.cnt >= 2; }
     // Counts and escapes when no lane of the warp holds more than one escape.
     static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
-                                                           uint16_t* ent, const uint16_t*) {
+                                                           uint16_t* ent, const uint8_t* in) {
         const uint32_t lane = threadIdx.x & 31;
         const uint32_t has = __ballot_sync(0xFFFFFFFFu, kp.cnt != 0);
         if (lane == 0) row[slot(0)] = (uint16_t)__popc(has);
-        if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent, nullptr);
+        if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent, in);
     }
 
+    // The lane's first escapes, from rank excl on, into the segment's entries;
+    // in: the tile's input (this lane's 32 elements at byte 32 t).
     static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent,
-                                                const uint16_t*) {
-        if (!kp.cnt) return;
+                                                const uint8_t* in) {
         const uint32_t lane = threadIdx.x & 31;
-        uint32_t g = excl;
+        const uint8_t* x = in + 32 * threadIdx.x;
         uint16_t* e = ent + slot(0) * kSegCap;
-#pragma unroll
-        for (int m = 0; m < 8; m++) {
-            if (!(kp.ent[m] & 0x10101010u)) continue;
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                if ((kp.ent[m] >> (8 * b)) & kMissEntry) {
-                    if (g < (uint32_t)kSegCap)
-                        e[g] = (uint16_t)((32 * lane + 4 * m + b) | (((kp.w[m] >> (8 * b + 2)) & kExpMask) << kOffBits));
-                    g++;
-                }
-            }
+        uint32_t g = excl;
+        for (uint32_t m = kp.mm; m && g < (uint32_t)kSegCap; m &= m - 1) {
+            const uint32_t j = __ffs(m) - 1;
+            e[g++] = (uint16_t)((32 * lane + j) | ((((uint32_t)x[j] >> 2) & kExpMask) << kOffBits));
         }
     }
 
@@ -516,22 +509,17 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
     for (uint32_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
         const uint32_t t0 = tile * (uint32_t)kTileElems;
         typename F::Keep kp;
-        const uint16_t* in;  // the tile's input, for formats that read escapes from it
+        const uint8_t* in;  // the tile's input, from which the escapes are read
         if (tile < full_tiles) {
             cp_async_wait<S - 1>();  // this tile's group (the oldest pending) has landed
             if (F::kSharedStage) __syncwarp();  // the warp's copies, visible to all its lanes
             F::compute_full(a, tables, t0, ring + slot * L * kThreads, kp);
-            in = reinterpret_cast<const uint16_t*>(ring + slot * L * kThreads);
+            in = reinterpret_cast<const uint8_t*>(ring + slot * L * kThreads);
         } else {
             F::process_partial(a, tables, t0, kp);
-            in = reinterpret_cast<const uint16_t*>(a.x) + t0;
+            in = a.x + (size_t)t0 * F::kElemBytes;
         }
-        // A format that reads its escapes from the stage refills it after the
-        // bookkeeping; the others refill it first.
-        if (!F::kEmitFromInput) {
-            if (F::kSharedStage) __syncwarp();  // every lane has read the stage before the refill
-            fill(tile + S * gridDim.x, slot);
-        }
+        // The bookkeeping reads escapes from the stage: refill after it.
         uint16_t* row = p.seg_cnt + (size_t)tile * kSegsMax;
         uint16_t* ent = p.seg_ent + (size_t)tile * kEntries;
         if (!__any_sync(0xFFFFFFFFu, F::multi(kp))) {
@@ -542,10 +530,8 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
             if (lane == 0) F::store_counts(row, e31, p31);
             if (kp.cnt) F::emit(kp, excl, ent, in);
         }
-        if (F::kEmitFromInput) {
-            if (F::kSharedStage) __syncwarp();
-            fill(tile + S * gridDim.x, slot);
-        }
+        if (F::kSharedStage) __syncwarp();  // every lane has read the stage before the refill
+        fill(tile + S * gridDim.x, slot);
         slot = slot + 1 == S ? 0 : slot + 1;
     }
     cp_async_wait<0>();
