@@ -16,8 +16,10 @@
 //     ahead (chunk_off at a chunk start, else a warp-wide search of the
 //     ascending positions inside the chunk) and its first 32 escapes are
 //     loaded one segment ahead;
-//   - each lane decodes its exponents in registers: codebook lookup by byte
-//     permutes (the 16 entries live in four registers);
+//   - each lane decodes its exponents in registers: BF16 two codes at a time
+//     from a 256-entry shared-memory table of code bytes (built per CTA from
+//     the codebook), E5M2 four at a time by byte permutes of the 16 entries
+//     held in four registers;
 //   - a segment with escapes parks its exponent words in shared memory, each
 //     lane holding an escape overwrites that element's exponent byte, and the
 //     words are read back (escapes beyond the first 32 of a segment are read
@@ -47,6 +49,37 @@ __device__ __forceinline__ uint32_t cb_lookup4(const uint32_t (&cb)[4], uint32_t
     return (hi & m) | (lo & ~m);
 }
 
+// Exponents of all 256 code bytes, two per entry (code byte c holds one
+// element in its low nibble, the next in its high nibble): entry c is
+// F::exp_byte(cb[c & 15]) | F::exp_byte(cb[c >> 4]) << 8.  One entry per
+// thread of the CTA; all threads call it before any returns.
+template <class F>
+__device__ __forceinline__ void build_pairs(uint16_t* t, const uint32_t (&cbw)[4]) {
+    static_assert(kThreads == 256, "one pair-table entry per thread");
+    const uint32_t c = threadIdx.x;
+    auto cb = [&](uint32_t k) {  // static word selects keep the parameters out of local memory
+        const uint32_t q = k >> 2;
+        const uint32_t w = q == 0 ? cbw[0] : q == 1 ? cbw[1] : q == 2 ? cbw[2] : cbw[3];
+        return F::exp_byte((w >> (8 * (k & 3u))) & 0xFFu);
+    };
+    t[c] = (uint16_t)(cb(c & 15u) | (cb(c >> 4) << 8));
+    __syncthreads();
+}
+
+// The codebook as each format's decode reads it: BF16 through the pair table
+// in shared memory, E5M2 from four registers holding F::exp_byte of each entry
+// (its segments already stream through shared memory, and more shared-memory
+// loads measured slower there).
+struct Luts {
+    const uint16_t* pairs;
+    uint32_t cb[4];
+};
+
+// Four exponent bytes of the four codes in c16 (two code bytes).
+__device__ __forceinline__ uint32_t pair_lookup4(const uint16_t* t, uint32_t c16) {
+    return __byte_perm(t[c16 & 0xFFu], t[(c16 >> 8) & 0xFFu], 0x5410);
+}
+
 // Four BF16 values from four sign+mantissa bytes and four exponent bytes.
 __device__ __forceinline__ uint2 assemble_bf16(uint32_t sm, uint32_t ex) {
     const uint32_t lo = (sm & 0x7F7F7F7Fu) | ((ex << 7) & 0x80808080u);
@@ -55,11 +88,11 @@ __device__ __forceinline__ uint2 assemble_bf16(uint32_t sm, uint32_t ex) {
 }
 
 // Four E5M2 values from four 3-bit fields (12 bits, field k at bits 3k) and
-// four exponent bytes.
-__device__ __forceinline__ uint32_t assemble_e5m2(uint32_t f12, uint32_t ex) {
+// four exponents already in place (bits 2..6 of each byte).
+__device__ __forceinline__ uint32_t assemble_e5m2(uint32_t f12, uint32_t ex2) {
     const uint32_t t = (f12 & 0x3Fu) | ((f12 & 0xFC0u) << 10);
     const uint32_t f = (t & 0x00070007u) | ((t & 0x00380038u) << 5);
-    return ((f << 5) & 0x80808080u) | ((ex << 2) & 0x7C7C7C7Cu) | (f & 0x03030303u);
+    return ((f << 5) & 0x80808080u) | ex2 | (f & 0x03030303u);
 }
 
 // First index j in [b, e) with pos[j] >= r, for positions in ascending order
@@ -159,7 +192,7 @@ __device__ __forceinline__ void patch_escapes(const DecodeArgs& a, const EscBatc
         if (local != 0xFFFFFFFFu) {
             uint32_t q, l, byte;
             F::locate(local, q, l, byte);
-            reinterpret_cast<uint8_t*>(pex)[(q * 32 + l) * 4 + byte] = (uint8_t)e.val;
+            reinterpret_cast<uint8_t*>(pex)[(q * 32 + l) * 4 + byte] = (uint8_t)F::exp_byte(e.val);
         }
     };
     put(eb);
@@ -197,14 +230,14 @@ constexpr size_t decode_smem_bytes() {
 //                                 `local` of the segment
 //   store(a, s0, s1, lane, d, ex)
 template <class F>
-__device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* smem) {
+__device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* smem,
+                                                const Luts& lut) {
     constexpr int S = kDecodeStages;
     constexpr uint32_t kPieces = F::kStageBytes / 16;
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t warps = gridDim.x * kWarps;
     const uint32_t nseg = (uint32_t)(((uint64_t)a.n + F::kSeg - 1) / F::kSeg);  // n may be 2^32 - 1
     const uint32_t full_segs = a.n / (uint32_t)F::kSeg;
-    const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
     uint8_t* ring = smem + (size_t)warp * F::kStageBytes;  // stage s at ring + s * kWarps * kStageBytes
     uint32_t* pex = reinterpret_cast<uint32_t*>(smem + (size_t)S * kWarps * F::kStageBytes) +
                     (size_t)warp * F::kExWords * 32;
@@ -265,7 +298,7 @@ __device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* sm
             d = F::load(a, s0, lane);
         }
         typename F::Ex ex;
-        F::decode(cb, d, ex);
+        F::decode(lut, d, ex);
         if (lo < hi) patch_escapes<F>(a, eb, lo, hi, s0, s1, pex, ex);  // warp-uniform
         if (more) eb = load_batch(a, lo1, hi1);
         F::store(a, s0, s1, lane, d, ex);
@@ -285,11 +318,11 @@ __device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* sm
 // The same segment loop with the next segment's dense words prefetched into
 // registers instead of a shared-memory ring (one segment ahead).
 template <class F>
-__device__ __forceinline__ void decode_segments_regs(const DecodeArgs& a, uint8_t* smem) {
+__device__ __forceinline__ void decode_segments_regs(const DecodeArgs& a, uint8_t* smem,
+                                                     const Luts& lut) {
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t warps = gridDim.x * kWarps;
     const uint32_t nseg = (uint32_t)(((uint64_t)a.n + F::kSeg - 1) / F::kSeg);  // n may be 2^32 - 1
-    const uint32_t cb[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
     uint32_t* pex = reinterpret_cast<uint32_t*>(smem) + (size_t)warp * F::kExWords * 32;
     uint32_t seg = blockIdx.x * kWarps + warp;
     if (seg >= nseg) return;  // warp-uniform
@@ -315,7 +348,7 @@ __device__ __forceinline__ void decode_segments_regs(const DecodeArgs& a, uint8_
             bounds(next, lo_n, hi_n);
         }
         typename F::Ex ex;
-        F::decode(cb, d, ex);
+        F::decode(lut, d, ex);
         if (lo < hi) patch_escapes<F>(a, eb, lo, hi, s0, s1, pex, ex);  // warp-uniform
         if (more) eb = load_batch(a, lo_n, hi_n);
         F::store(a, s0, s1, lane, d, ex);
@@ -377,11 +410,13 @@ struct Bf16Seg {
         }
         return d;
     }
-    static __device__ __forceinline__ void decode(const uint32_t (&cb)[4], const Dense& d, Ex& ex) {
+    static constexpr bool kPairs = true;  // exponents from the pair table
+    static __device__ __forceinline__ uint32_t exp_byte(uint32_t e) { return e; }
+    static __device__ __forceinline__ void decode(const Luts& lut, const Dense& d, Ex& ex) {
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
-            ex.e[2 * k] = cb_lookup4(cb, d.code[k] & 0xFFFFu);
-            ex.e[2 * k + 1] = cb_lookup4(cb, d.code[k] >> 16);
+            ex.e[2 * k] = pair_lookup4(lut.pairs, d.code[k] & 0xFFFFu);
+            ex.e[2 * k + 1] = pair_lookup4(lut.pairs, d.code[k] >> 16);
         }
     }
     static __device__ __forceinline__ void locate(uint32_t local, uint32_t& q, uint32_t& l,
@@ -474,13 +509,16 @@ struct E5m2Seg {
         }
         return d;
     }
-    static __device__ __forceinline__ void decode(const uint32_t (&cb)[4], const Dense& d, Ex& ex) {
+    // Exponents enter the words already shifted to bits 2..6 of the byte.
+    static constexpr bool kPairs = false;  // exponents from the codebook registers
+    static __device__ __forceinline__ uint32_t exp_byte(uint32_t e) { return (e << 2) & 0x7Cu; }
+    static __device__ __forceinline__ void decode(const Luts& lut, const Dense& d, Ex& ex) {
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
             const uint32_t cw[4] = {d.code[k].x, d.code[k].y, d.code[k].z, d.code[k].w};
 #pragma unroll
             for (int m = 0; m < 8; m++)
-                ex.e[8 * k + m] = cb_lookup4(cb, (cw[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
+                ex.e[8 * k + m] = cb_lookup4(lut.cb, (cw[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
         }
     }
     static __device__ __forceinline__ void locate(uint32_t local, uint32_t& q, uint32_t& l,
@@ -521,8 +559,18 @@ struct E5m2Seg {
 template <class F>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    if constexpr (F::kRing) decode_segments<F>(a, smem);
-    else decode_segments_regs<F>(a, smem);
+    __shared__ uint16_t pairs[256];
+    Luts lut;
+    lut.pairs = pairs;
+    if constexpr (F::kPairs) build_pairs<F>(pairs, a.cbw);
+#pragma unroll
+    for (int q = 0; q < 4; q++) {  // F::exp_byte of each byte of the codebook words
+        const uint32_t w = a.cbw[q];
+        lut.cb[q] = F::exp_byte(w & 0xFFu) | (F::exp_byte((w >> 8) & 0xFFu) << 8) |
+                    (F::exp_byte((w >> 16) & 0xFFu) << 16) | (F::exp_byte(w >> 24) << 24);
+    }
+    if constexpr (F::kRing) decode_segments<F>(a, smem, lut);
+    else decode_segments_regs<F>(a, smem, lut);
 }
 
 template <class F>
