@@ -411,6 +411,7 @@ struct Bf16Seg {
         return d;
     }
     static constexpr bool kPairs = true;  // exponents from the pair table
+    static constexpr int kMinBlocks = 4;  // resident CTAs per SM: 64 registers
     static __device__ __forceinline__ uint32_t exp_byte(uint32_t e) { return e; }
     static __device__ __forceinline__ void decode(const Luts& lut, const Dense& d, Ex& ex) {
 #pragma unroll
@@ -511,6 +512,7 @@ struct E5m2Seg {
     }
     // Exponents enter the words already shifted to bits 2..6 of the byte.
     static constexpr bool kPairs = false;  // exponents from the codebook registers
+    static constexpr int kMinBlocks = 5;  // resident CTAs per SM: 48 registers, 1.4% faster than 4
     static __device__ __forceinline__ uint32_t exp_byte(uint32_t e) { return (e << 2) & 0x7Cu; }
     static __device__ __forceinline__ void decode(const Luts& lut, const Dense& d, Ex& ex) {
 #pragma unroll
@@ -557,7 +559,7 @@ struct E5m2Seg {
 };
 
 template <class F>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, F::kMinBlocks) decode_kernel(const DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint16_t pairs[256];
     Luts lut;
