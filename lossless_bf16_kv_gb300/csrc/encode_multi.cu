@@ -14,20 +14,22 @@
 //                ring, field split, code lookup in shared-memory word tables,
 //                dense code and sign+mantissa stores.  Each warp ranks the
 //                escapes of its segments (ballots when no group holds two
-//                escapes, else one shuffle scan) and stores the counts and
-//                the first few escapes of every segment in the workspace.
+//                escapes, else one shuffle scan) and stores the segments'
+//                counts and its first 32 escapes, as one list in element order
+//                within each segment, in the workspace.
 //   K2 prefix    exclusive prefix of the per-tile escape counts (sums of the
 //                segment counts; 2048 tiles per CTA,
 //                decoupled look-back across CTAs, bounded waits); E.
 //   K3 place     a warp per tile (BF16) or four (E5M2): segment offsets by
 //                shuffle scan, escapes
 //                copied to their final places, chunk offsets at chunk starts.
-//                A segment with more escapes than its workspace share is
+//                A segment whose escapes do not all fit in its warp's list is
 //                rebuilt from the input in element order.
 // Segments: BF16 -- the 256 consecutive elements warp w covers with its group
-// k (element order 8k + w, workspace slot 4w + k), 8 workspace entries each;
-// E5M2 -- the 1024 elements of warp w, 32 entries each.  Entries hold the
-// position in the segment and the raw exponent.
+// k (element order 8k + w, count slot 4w + k); warp w's list holds its four
+// segments' escapes in order k = 0..3.  E5M2 -- the 1024 elements of warp w,
+// the whole list.  Entries hold the position in the segment and the raw
+// exponent.
 #include <cstdint>
 
 #include "common.cuh"
@@ -41,6 +43,7 @@ namespace {
 constexpr int kTileElems = 8192;     // elements per tile (K1 CTA / K3 warp)
 constexpr int kSegsMax = 32;         // segment slots per tile in the workspace
 constexpr int kEntries = 256;        // escape entries per tile in the workspace
+constexpr int kWarpCap = kEntries / kWarps;  // 32: entries of one warp's escape list
 constexpr int kScanTiles = 2048;     // tiles per K2 CTA (8 per thread)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -51,18 +54,6 @@ struct MultiPtrs {
     uint16_t* seg_cnt;
     uint16_t* seg_ent;
 };
-
-__device__ __forceinline__ void build_table(uint8_t* table, const uint32_t (&cbw)[4]) {
-    const int tid = threadIdx.x;
-    table[tid] = (uint8_t)kMissEntry;
-    __syncthreads();
-    // Static indices only: a dynamic index into the kernel parameters would
-    // make the compiler copy them to local memory.
-    const uint32_t q = (uint32_t)tid >> 2;
-    const uint32_t w = q == 0 ? cbw[0] : q == 1 ? cbw[1] : q == 2 ? cbw[2] : cbw[3];
-    if (tid < 16) table[(w >> (8 * (tid & 3))) & 0xFFu] = (uint8_t)tid;
-    __syncthreads();
-}
 
 // Warp-wide exclusive scan of one word per lane, excl = sum of p over the
 // lower lanes.  Also returns lane 31's exclusive prefix and word, from which
@@ -101,7 +92,6 @@ struct Bf16Dense {
     static constexpr int kGroups = 4;
     static constexpr int kSegs = 32;
     static constexpr int kSegLen = 256;
-    static constexpr int kSegCap = kEntries / kSegs;  // 8
     static constexpr int kOffBits = 8;
     static constexpr uint32_t kExpMask = 0xFFu;
     struct Tables {
@@ -120,14 +110,6 @@ struct Bf16Dense {
     // slot 4w + k, so that a warp's four counts are one 8-byte store.
     static __device__ __forceinline__ uint32_t slot(int k) { return (threadIdx.x >> 5) * 4 + k; }
     static __device__ __forceinline__ uint32_t storage(uint32_t s) { return (s & 7u) * 4 + (s >> 3); }
-    // Lane 0 stores the warp's four segment totals (16 bits each).
-    static __device__ __forceinline__ void store_counts(uint16_t* row, uint32_t e31, uint32_t p31) {
-        const uint32_t t02 = (e31 & 0x00FF00FFu) + (p31 & 0x00FF00FFu);
-        const uint32_t t13 = ((e31 >> 8) & 0x00FF00FFu) + ((p31 >> 8) & 0x00FF00FFu);
-        *reinterpret_cast<uint2*>(row + slot(0)) =
-            make_uint2(__byte_perm(t02, t13, 0x5410), __byte_perm(t02, t13, 0x7632));
-    }
-
     static __device__ __forceinline__ void build_tables(Tables& tb, const uint32_t (&cbw)[4]) {
         const uint32_t tid = threadIdx.x;
 #pragma unroll
@@ -244,6 +226,11 @@ struct Bf16Dense {
     static __device__ __forceinline__ bool multi(const Keep& kp) {
         return (kp.cnt & 0xFEFEFEFEu) != 0;
     }
+    // Escape entries go to the warp's list of kWarpCap entries, ordered by
+    // group k, then lane, then element (so a tile's escapes fill a few
+    // sectors): an escape's rank is its group's base (the escapes of the
+    // warp's lower groups) plus its rank within the group.
+    //
     // Counts and escapes when no group of the warp holds more than one escape
     // (almost every tile at KV-cache escape rates): a group's rank is the
     // number of lower lanes whose same group has an escape, a segment's total
@@ -254,31 +241,51 @@ struct Bf16Dense {
         uint32_t has[kGroups];
 #pragma unroll
         for (int k = 0; k < kGroups; k++) has[k] = __ballot_sync(0xFFFFFFFFu, kp.miss[k] != 0);
+        const uint32_t c0 = __popc(has[0]), c1 = __popc(has[1]), c2 = __popc(has[2]);
         if (lane == 0)
             *reinterpret_cast<uint2*>(row + slot(0)) =
-                make_uint2(__popc(has[0]) | (__popc(has[1]) << 16), __popc(has[2]) | (__popc(has[3]) << 16));
+                make_uint2(c0 | (c1 << 16), c2 | (__popc(has[3]) << 16));
         if (kp.cnt) {
             uint32_t excl = 0;
 #pragma unroll
             for (int k = 0; k < kGroups; k++) excl |= (uint32_t)__popc(has[k] & lt) << (8 * k);
-            emit(kp, excl, ent, in);
+            const uint32_t base[kGroups] = {0u, c0, c0 + c1, c0 + c1 + c2};
+            emit(kp, excl, base, ent, in);
+        }
+    }
+    // Counts and escapes in general: one packed warp scan of the four groups'
+    // counts.
+    static __device__ __forceinline__ void bookkeep_multi(const Keep& kp, uint16_t* row,
+                                                          uint16_t* ent, const uint8_t* in) {
+        uint32_t excl, e31, p31;
+        warp_scan_excl(kp.cnt, excl, e31, p31);
+        const uint32_t t02 = (e31 & 0x00FF00FFu) + (p31 & 0x00FF00FFu);  // totals of groups 0, 2
+        const uint32_t t13 = ((e31 >> 8) & 0x00FF00FFu) + ((p31 >> 8) & 0x00FF00FFu);  // 1, 3
+        if ((threadIdx.x & 31) == 0)
+            *reinterpret_cast<uint2*>(row + slot(0)) =
+                make_uint2(__byte_perm(t02, t13, 0x5410), __byte_perm(t02, t13, 0x7632));
+        if (kp.cnt) {
+            const uint32_t c0 = t02 & 0xFFFFu, c1 = t13 & 0xFFFFu, c2 = t02 >> 16;
+            const uint32_t base[kGroups] = {0u, c0, c0 + c1, c0 + c1 + c2};
+            emit(kp, excl, base, ent, in);
         }
     }
 
-    // The first kSegCap escapes of each segment into its workspace entries.
-    // excl: the exclusive escape ranks of this lane's groups, one per byte.
-    // in: the tile's input (group k of this thread at element loff(k)).
-    static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent,
+    // The warp's first kWarpCap escapes into its list.  excl: the exclusive
+    // escape ranks of this lane's groups, one per byte; base: the groups'
+    // bases; in: the tile's input (group k of this thread at element loff(k)).
+    static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl,
+                                                const uint32_t (&base)[kGroups], uint16_t* ent,
                                                 const uint8_t* in) {
         const uint32_t lane = threadIdx.x & 31;
+        uint16_t* e = ent + (threadIdx.x >> 5) * kWarpCap;
 #pragma unroll
         for (int k = 0; k < kGroups; k++) {
             uint32_t m = kp.miss[k];
             if (!m) continue;
-            uint32_t g = (excl >> (8 * k)) & 0xFFu;
-            uint16_t* e = ent + slot(k) * kSegCap;
+            uint32_t g = base[k] + ((excl >> (8 * k)) & 0xFFu);
             const uint16_t* x = reinterpret_cast<const uint16_t*>(in) + loff(k);
-            while (m && g < (uint32_t)kSegCap) {
+            while (m && g < (uint32_t)kWarpCap) {
                 const uint32_t b = __ffs(m) - 1;  // bit b: element (b & 3) + 4 * (b >> 4)
                 m &= m - 1;
                 const uint32_t j = (b & 3u) + ((b >> 4) << 2);
@@ -286,6 +293,18 @@ struct Bf16Dense {
                 e[g++] = (uint16_t)((8 * lane + j) | (ex << kOffBits));
             }
         }
+    }
+
+    // Warp list of segment s (element order 8k + w) and, from the counts held
+    // by the lanes of its tile (lane base + s holds segment s; all lanes call
+    // it), the entries of the warp's lower groups that precede it there.
+    static __device__ __forceinline__ uint32_t seg_list(uint32_t s) { return s & 7u; }
+    static __device__ __forceinline__ uint32_t seg_base(uint32_t s, uint32_t cnt, uint32_t lbase) {
+        const uint32_t w = s & 7u, k = s >> 3;
+        const uint32_t n0 = __shfl_sync(0xFFFFFFFFu, cnt, lbase + w);
+        const uint32_t n1 = __shfl_sync(0xFFFFFFFFu, cnt, lbase + 8 + w);
+        const uint32_t n2 = __shfl_sync(0xFFFFFFFFu, cnt, lbase + 16 + w);
+        return (k > 0 ? n0 : 0u) + (k > 1 ? n1 : 0u) + (k > 2 ? n2 : 0u);
     }
 
     // Exponent of element i of the input (K3's rebuild of a full segment).
@@ -301,7 +320,6 @@ struct Bf16Dense {
 struct E5m2Dense {
     static constexpr int kSegs = kWarps;              // 8
     static constexpr int kSegLen = 1024;
-    static constexpr int kSegCap = kEntries / kSegs;  // 32
     static constexpr int kOffBits = 10;
     static constexpr uint32_t kExpMask = 0x1Fu;
     // Code table indexed by the raw byte with its sign bit cleared (exponent
@@ -340,9 +358,6 @@ struct E5m2Dense {
     }
     static __device__ __forceinline__ uint32_t slot(int) { return threadIdx.x >> 5; }
     static __device__ __forceinline__ uint32_t storage(uint32_t s) { return s; }
-    static __device__ __forceinline__ void store_counts(uint16_t* row, uint32_t e31, uint32_t p31) {
-        row[slot(0)] = (uint16_t)(e31 + p31);
-    }
 
     // Input words of a full tile.  Warp w's 1 KiB (elements 1024w..1024w+1023)
     // arrives as 64 pieces of 16 bytes, lane l copying pieces l and 32 + l of
@@ -449,15 +464,26 @@ struct E5m2Dense {
         if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent, in);
     }
 
+    static __device__ __forceinline__ void bookkeep_multi(const Keep& kp, uint16_t* row,
+                                                          uint16_t* ent, const uint8_t* in) {
+        uint32_t excl, e31, p31;
+        warp_scan_excl(kp.cnt, excl, e31, p31);
+        if ((threadIdx.x & 31) == 0) row[slot(0)] = (uint16_t)(e31 + p31);
+        if (kp.cnt) emit(kp, excl, ent, in);
+    }
+    // One segment per warp: segment s's entries are warp s's whole list.
+    static __device__ __forceinline__ uint32_t seg_list(uint32_t s) { return s; }
+    static __device__ __forceinline__ uint32_t seg_base(uint32_t, uint32_t, uint32_t) { return 0u; }
+
     // The lane's first escapes, from rank excl on, into the segment's entries;
     // in: the tile's input (this lane's 32 elements at byte 32 t).
     static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent,
                                                 const uint8_t* in) {
         const uint32_t lane = threadIdx.x & 31;
         const uint8_t* x = in + 32 * threadIdx.x;
-        uint16_t* e = ent + slot(0) * kSegCap;
+        uint16_t* e = ent + slot(0) * kWarpCap;
         uint32_t g = excl;
-        for (uint32_t m = kp.mm; m && g < (uint32_t)kSegCap; m &= m - 1) {
+        for (uint32_t m = kp.mm; m && g < (uint32_t)kWarpCap; m &= m - 1) {
             const uint32_t j = __ffs(m) - 1;
             e[g++] = (uint16_t)((32 * lane + j) | ((((uint32_t)x[j] >> 2) & kExpMask) << kOffBits));
         }
@@ -492,7 +518,6 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
     extern __shared__ uint4 ring[];  // [S][L][kThreads]
     __shared__ typename F::Tables tables;
     F::build_tables(tables, a.cbw);
-    const uint32_t tid = threadIdx.x, lane = tid & 31;
     const uint32_t full_tiles = a.n / (uint32_t)kTileElems;
     auto fill = [&](uint32_t tile, int slot) {
         if (tile < full_tiles) {
@@ -525,10 +550,7 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
         if (!__any_sync(0xFFFFFFFFu, F::multi(kp))) {
             F::bookkeep_single(kp, row, ent, in);
         } else {
-            uint32_t excl, e31, p31;
-            warp_scan_excl(kp.cnt, excl, e31, p31);
-            if (lane == 0) F::store_counts(row, e31, p31);
-            if (kp.cnt) F::emit(kp, excl, ent, in);
+            F::bookkeep_multi(kp, row, ent, in);
         }
         if (F::kSharedStage) __syncwarp();  // every lane has read the stage before the refill
         fill(tile + S * gridDim.x, slot);
@@ -648,15 +670,27 @@ __device__ __forceinline__ void put_escape(const EncodeArgs& a, uint32_t g, uint
     }
 }
 
+// Whether exponent e (< 256) is one of the 16 codebook entries, four per word:
+// some byte of cbw[q] ^ (e in every byte) is zero.
+__device__ __forceinline__ bool in_codebook(const uint32_t (&cbw)[4], uint32_t e) {
+    const uint32_t rep = e * 0x01010101u;
+    uint32_t z = 0;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const uint32_t t = cbw[q] ^ rep;
+        z |= (t - 0x01010101u) & ~t & 0x80808080u;  // nonzero iff t has a zero byte
+    }
+    return z != 0;
+}
+
 // A warp places the escapes of 32 / kSegs consecutive tiles (BF16: one, E5M2:
 // four), lane l taking segment l mod kSegs (element order) of tile l / kSegs.
 template <class F>
-__global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, const MultiPtrs p,
-                                                         uint32_t num_tiles) {
+__global__ void __launch_bounds__(kThreads, 8) place_kernel(const EncodeArgs a, const MultiPtrs p,
+                                                            uint32_t num_tiles) {
     constexpr uint32_t kOffMask = (1u << F::kOffBits) - 1u;
     constexpr uint32_t SEGS = F::kSegs, TPW = 32 / F::kSegs;
-    __shared__ uint8_t table[256];
-    build_table(table, a.cbw);
+    const uint32_t cbw[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW;
     if (tile0 >= num_tiles) return;  // warp-uniform
@@ -678,14 +712,16 @@ __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, con
     const uint32_t first = __shfl_sync(0xFFFFFFFFu, incl - cnt, lane & ~(SEGS - 1));
     const uint32_t off = incl - cnt - first;
     const uint16_t* ent = p.seg_ent + (size_t)tile * kEntries;
+    // Where this lane's segment's entries start in its warp list.
+    const uint32_t sbase = F::seg_base(sgl, cnt, lane & ~(SEGS - 1));
 
     // Escapes of segment sgl of this lane's tile, in element order.
     if (cnt) {
         const uint32_t s0 = sgl * F::kSegLen;
         const uint32_t g0 = excl + off;
-        if (cnt <= (uint32_t)F::kSegCap) {
+        if (sbase + cnt <= (uint32_t)kWarpCap) {
             for (uint32_t r = 0; r < cnt; r++) {
-                const uint32_t e = ent[F::storage(sgl) * F::kSegCap + r];
+                const uint32_t e = ent[F::seg_list(sgl) * kWarpCap + sbase + r];
                 const uint32_t x = r0 + s0 + (e & kOffMask);
                 put_escape(a, g0 + r, x - chunk_quot(a.cdiv, x) * a.cdiv.d, e >> F::kOffBits);
             }
@@ -695,7 +731,7 @@ __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, con
             uint32_t g = g0;
             for (uint32_t l = s0; l < end; l++) {
                 const uint32_t e = F::exponent_at(a, t0 + l);
-                if (table[e] & kMissEntry) {
+                if (!in_codebook(cbw, e)) {
                     const uint32_t x = r0 + l;
                     put_escape(a, g++, x - chunk_quot(a.cdiv, x) * a.cdiv.d, e);
                 }
@@ -704,7 +740,16 @@ __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, con
     }
 
     // chunk_off at every chunk start of each of the warp's tiles: the exclusive
-    // escape rank of the chunk's first element.
+    // escape rank of the chunk's first element.  When the chunk size is a
+    // multiple of the segment length every chunk start inside a tile is a
+    // segment start (tiles and segments start at multiples of it), and the
+    // lane of that segment writes it from its own offset.
+    if (a.cdiv.d % (uint32_t)F::kSegLen == 0) {
+        const uint32_t s0 = sgl * F::kSegLen, x = r0 + s0;  // x < d + kTileElems
+        const uint32_t qx = chunk_quot(a.cdiv, x);
+        if (tvalid && s0 < len && x == qx * a.cdiv.d) a.chunk_off[q0 + qx] = excl + off;
+        return;
+    }
     for (uint32_t t = 0; t < TPW; t++) {
         const uint32_t tl = tile0 + t;
         if (tl >= num_tiles) break;  // warp-uniform
@@ -721,16 +766,17 @@ __global__ void __launch_bounds__(kThreads) place_kernel(const EncodeArgs a, con
             const uint32_t sg = bl / F::kSegLen;
             const uint32_t o = __shfl_sync(0xFFFFFFFFu, off, t * SEGS + sg);
             const uint32_t c = __shfl_sync(0xFFFFFFFFu, cnt, t * SEGS + sg);
+            const uint32_t bb = __shfl_sync(0xFFFFFFFFu, sbase, t * SEGS + sg);
             if (valid) {
                 const uint32_t lim = bl - sg * F::kSegLen;
                 uint32_t rank = 0;
                 if (lim == 0) {
-                } else if (c <= (uint32_t)F::kSegCap) {
-                    const uint16_t* es = uent + F::storage(sg) * F::kSegCap;
+                } else if (bb + c <= (uint32_t)kWarpCap) {
+                    const uint16_t* es = uent + F::seg_list(sg) * kWarpCap + bb;
                     for (uint32_t r = 0; r < c; r++) rank += (es[r] & kOffMask) < lim;
                 } else {
                     for (uint32_t l = sg * F::kSegLen; l < bl; l++)
-                        rank += (table[F::exponent_at(a, u0 + l)] & kMissEntry) != 0;
+                        rank += !in_codebook(cbw, F::exponent_at(a, u0 + l));
                 }
                 a.chunk_off[uq0 + q] = uexcl + o + rank;
             }
