@@ -87,11 +87,14 @@ def test_small_shapes(fmt, chunk):
 @pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
 def test_multi_tile_ragged(fmt):
     # Several encode/decode tiles plus a ragged tail, chunk sizes that do and
-    # do not divide the tile.
+    # do not divide the tile.  256, 512, 2048 and 12288 are multiples of the
+    # BF16 encode segment (256 elements), 2048 and 12288 of the E5M2 one
+    # (1024), and 12288 spans tiles (8192): chunk offsets come from the
+    # segment-start path there and from the general path otherwise.
     dt = torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2
     x = synth.kv_cache(1, 777, seed=3, device=DEV, dtype=dt).reshape(-1)[:1_500_007]
     cb, _ = gpu_calibrate(synth.kv_cache(1, 64, seed=1, device=DEV, dtype=dt))
-    for chunk in (8, 40, 1000, 1024, 3000, 65536):
+    for chunk in (8, 40, 256, 512, 1000, 1024, 2048, 3000, 12288, 65536):
         check_roundtrip(x, chunk, cb, f"{fmt} ragged chunk {chunk}")
 
 
@@ -102,6 +105,34 @@ def test_zero_and_all_escape_tensors():
     ones = torch.ones(50000, dtype=torch.bfloat16, device=DEV)    # exponent 127: none
     cb2 = list(range(120, 136))
     assert check_roundtrip(ones, 1024, cb2, "no escapes") == 0
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
+def test_warp_escape_list_boundary(fmt):
+    """Encode keeps each warp's first 32 escapes of a tile in one list (BF16:
+    its four 256-element segments, at tile offsets 256w + 2048k, in order k;
+    E5M2: its 1024 elements) and rebuilds a segment that does not fit from
+    the input.  Tile 0 fills warp 0's list exactly, tile 1 overflows it by
+    one in its last flagged segment; the streams must still be the oracle's."""
+    n = 3 * 8192 + 123
+    if fmt == "bf16":
+        bits = torch.full((n,), 127 << 7, dtype=torch.int16)   # 1.0: exponent 127, in the codebook
+        esc = 27 << 7                                           # exponent 27, not in it
+        segs = [(0, 20), (2048, 12), (4096, 0)]                # tile 0: 32 escapes in warp 0
+        segs1 = [(0, 20), (2048, 12), (4096, 1)]               # tile 1: 33 (last one overflows)
+        cb, dt = list(range(120, 136)), torch.bfloat16
+    else:
+        bits = torch.full((n,), 15 << 2, dtype=torch.uint8)    # 1.0: exponent 15
+        esc = 5 << 2                                            # exponent 5
+        segs = [(0, 32)]                                        # warp 0's segment: exactly 32
+        segs1 = [(0, 33), (1024, 5)]                            # 33 in warp 0, 5 in warp 1
+        cb, dt = list(range(10, 26)), torch.float8_e5m2
+    for base, pattern in ((0, segs), (8192, segs1)):
+        for off, cnt in pattern:
+            bits[torch.arange(cnt) * 7 + base + off] = esc      # spread inside the segment
+    x = bits.view(dt).to(DEV)
+    for chunk in (1024, 1000, 8):                           # segment-start and general chunk paths
+        check_roundtrip(x, chunk, cb, f"{fmt} warp list boundary chunk {chunk}")
 
 
 def test_deterministic_and_workspace_reuse():
