@@ -35,18 +35,22 @@
 namespace splitzip {
 namespace {
 
-// Exponents of four codes (code k in nibble k of c16) from the codebook held
-// in four words (cb0 = entries 0..3, ..., cb3 = entries 12..15).  Entries
-// 0..7 and 8..15 are each one byte permute; a third permute in sign-replicate
-// mode turns bit 3 of each code into a 0x00/0xFF byte mask that picks between
-// the two.
-__device__ __forceinline__ uint32_t cb_lookup4(const uint32_t (&cb)[4], uint32_t c16) {
-    const uint32_t sel = c16 & 0x7777u;
-    const uint32_t lo = prmt(cb[0], cb[1], sel);
-    const uint32_t hi = prmt(cb[2], cb[3], sel);
-    const uint32_t t = c16 & 0x8888u;
-    const uint32_t m = prmt(0x00008000u, 0u, t | (t >> 3));  // nibble 9 -> 0xFF, 0 -> 0x00
-    return (hi & m) | (lo & ~m);
+// Exponents of the eight codes of a code word (code k in nibble k of cw)
+// from the codebook held in four words (cb0 = entries 0..3, ..., cb3 =
+// entries 12..15): codes 0..3 into lo, codes 4..7 into hi.  Entries 0..7 and
+// 8..15 are each one byte permute; a third permute in sign-replicate mode
+// turns bit 3 of each code into a 0x00/0xFF byte mask that picks between the
+// two.  The masks are formed once for all eight codes (a permute reads only
+// the low 16 bits of its selector).
+__device__ __forceinline__ void cb_lookup8(const uint32_t (&cb)[4], uint32_t cw, uint32_t& lo,
+                                           uint32_t& hi) {
+    const uint32_t sel = cw & 0x77777777u;
+    const uint32_t t = cw & 0x88888888u;
+    const uint32_t u = t | (t >> 3);  // nibble 9 where bit 3 is set, else 0
+    const uint32_t sh = sel >> 16, uh = u >> 16;
+    const uint32_t m0 = prmt(0x00008000u, 0u, u), m1 = prmt(0x00008000u, 0u, uh);
+    lo = (prmt(cb[2], cb[3], sel) & m0) | (prmt(cb[0], cb[1], sel) & ~m0);
+    hi = (prmt(cb[2], cb[3], sh) & m1) | (prmt(cb[0], cb[1], sh) & ~m1);
 }
 
 // Exponents of all 256 code bytes, two per entry (code byte c holds one
@@ -519,8 +523,7 @@ struct E5m2Seg {
         for (int k = 0; k < kGroups; k++) {
             const uint32_t cw[4] = {d.code[k].x, d.code[k].y, d.code[k].z, d.code[k].w};
 #pragma unroll
-            for (int m = 0; m < 8; m++)
-                ex.e[8 * k + m] = cb_lookup4(lut.cb, (cw[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
+            for (int i = 0; i < 4; i++) cb_lookup8(lut.cb, cw[i], ex.e[8 * k + 2 * i], ex.e[8 * k + 2 * i + 1]);
         }
     }
     static __device__ __forceinline__ void locate(uint32_t local, uint32_t& q, uint32_t& l,
