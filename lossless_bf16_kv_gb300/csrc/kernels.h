@@ -66,8 +66,8 @@ struct CalibArgs {
 //   tile_excl            4 bytes per tile: exclusive prefix of the tiles'
 //                        escape counts
 //   seg_cnt              32 x uint16 per tile: escapes per segment
-//   seg_ent              256 x uint16 per tile: the segments' first escapes
-//                        (position in segment | exponent << offset bits)
+//   seg_ent              256 x uint16 per tile: per warp, a list of its first
+//                        32 escapes (position in segment | exponent << offset bits)
 struct MultiLayout {
     size_t states, tile_excl, seg_cnt, seg_ent, bytes;
 };
