@@ -6,6 +6,8 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 namespace splitzip {
@@ -228,6 +230,51 @@ __device__ __forceinline__ void cp_async_wait() {
 // Named barrier over the first `threads` threads of the CTA (id 1..15).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ------------------------------------------------------- launch waves
+//
+// How many CTAs of kernel K fit on the current device at once: its SM count
+// times the CTAs of `threads` threads with `smem` bytes of dynamic shared
+// memory that one SM holds (K's dynamic shared-memory limit raised to smem
+// first).  Computed once per kernel and device, then taken from a cache, so
+// a call does not pay the attribute and occupancy queries each time.
+struct Wave {
+    int sms = 0;
+    int per_sm = 0;
+    uint64_t ctas() const { return (uint64_t)(sms > 0 ? sms : 1) * (uint64_t)(per_sm > 0 ? per_sm : 1); }
+};
+
+template <auto K>
+cudaError_t launch_wave(int threads, size_t smem, Wave& out) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static Wave cache[kMaxDevices];
+    static bool known[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    std::unique_lock<std::mutex> lock(mu, std::defer_lock);
+    if (cached) {
+        lock.lock();
+        if (known[dev]) {
+            out = cache[dev];
+            return cudaSuccess;
+        }
+    }
+    Wave w;
+    e = cudaDeviceGetAttribute(&w.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&w.per_sm, K, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (cached) {
+        cache[dev] = w;
+        known[dev] = true;
+    }
+    out = w;
+    return cudaSuccess;
 }
 
 }  // namespace splitzip

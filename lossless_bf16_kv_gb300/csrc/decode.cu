@@ -581,18 +581,12 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) decode_kernel(const D
 template <class F>
 cudaError_t launch_segments(const DecodeArgs& a, cudaStream_t s) {
     constexpr size_t smem = decode_smem_bytes<F>();
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(decode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<F>, kThreads, smem);
+    Wave wv;
+    const cudaError_t e = launch_wave<decode_kernel<F>>(kThreads, smem, wv);
     if (e != cudaSuccess) return e;
     const uint64_t nseg = ((uint64_t)a.n + F::kSeg - 1) / F::kSeg;
     const uint64_t ctas = (nseg + kWarps - 1) / kWarps;
-    const uint64_t wave = (uint64_t)(sms > 0 ? sms : 1) * (uint64_t)(per_sm > 0 ? per_sm : 1);
+    const uint64_t wave = wv.ctas();
     decode_kernel<F><<<(uint32_t)(ctas < wave ? ctas : wave), kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }

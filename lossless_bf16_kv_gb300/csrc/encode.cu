@@ -641,18 +641,11 @@ __global__ void __launch_bounds__(kEncodeThreads, 2) encode_kernel(const EncodeA
 template <class F>
 cudaError_t launch_pipeline(const EncodeArgs& a, cudaStream_t s) {
     constexpr size_t smem = sizeof(EncodeSmem<F::kElemBytes>);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    Wave wv;
+    const cudaError_t e = launch_wave<encode_kernel<F>>(kEncodeThreads, smem, wv);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(encode_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int sms = 0, per_sm = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<F>, kEncodeThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    const uint32_t grid = min(a.num_tiles, (uint32_t)(sms * per_sm));
+    if (wv.per_sm < 1) return cudaErrorInvalidConfiguration;
+    const uint32_t grid = min(a.num_tiles, (uint32_t)(wv.sms * wv.per_sm));
     encode_kernel<F><<<grid, kEncodeThreads, smem, s>>>(a);
     return cudaGetLastError();
 }

@@ -795,16 +795,10 @@ cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
     const uint32_t tiles = a.num_tiles;
     const uint32_t blocks = (tiles + kScanTiles - 1) / kScanTiles;
     constexpr size_t smem = dense_smem_bytes<F>();
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(dense_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dense_kernel<F>, kThreads, smem);
+    Wave wv;
+    cudaError_t e = launch_wave<dense_kernel<F>>(kThreads, smem, wv);
     if (e != cudaSuccess) return e;
-    const uint64_t wave = (uint64_t)(sms > 0 ? sms : 1) * (uint64_t)(per_sm > 0 ? per_sm : 1);
+    const uint64_t wave = wv.ctas();
     dense_kernel<F><<<(uint32_t)(tiles < wave ? tiles : wave), kThreads, smem, s>>>(a, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
