@@ -149,6 +149,35 @@ def _fmt_of(x: torch.Tensor, fmt: str | None) -> str:
     raise TypeError(f"unsupported dtype {x.dtype}")
 
 
+_ELEM = {"bf16": 2, "e5m2": 1}
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _need(t: torch.Tensor, nbytes: int, what: str):
+    """The C ABI takes plain pointers: check here that t holds nbytes."""
+    if _nbytes(t) < nbytes:
+        raise SplitZipError(ERR_INVALID_ARG, f"{what} holds {_nbytes(t)} bytes, {nbytes} needed")
+
+
+def _elements(x: torch.Tensor, fmt: str, what: str = "x") -> int:
+    """Element count of x in the format's element width (2 bytes BF16, 1 E5M2)."""
+    if fmt not in _ELEM:
+        raise ValueError(f"unknown format {fmt!r}")
+    if x.element_size() != _ELEM[fmt]:
+        raise SplitZipError(ERR_INVALID_ARG,
+                            f"{what} has {x.element_size()}-byte elements, {fmt} needs {_ELEM[fmt]}")
+    return x.numel()
+
+
+def _need_streams(s: dict, n: int, chunk: int, fmt: str):
+    _need(s["codes"], (n + 1) // 2, "codes")
+    _need(s["signman"], splitzip_signman_bytes(n, fmt), "signman")
+    _need(s["chunk_off"], 4 * (splitzip_num_chunks(n, chunk) + 1), "chunk_off")
+
+
 def _codebook(cb) -> Codebook:
     c = Codebook()
     vals = [int(v) for v in (cb.tolist() if hasattr(cb, "tolist") else cb)]
@@ -216,9 +245,11 @@ def splitzip_calibrate(x: torch.Tensor, workspace: torch.Tensor, fmt: str | None
                        stream=None):
     """Codebook (list of 16 ints) and coverage of x; synchronises the stream."""
     fmt = _fmt_of(x, fmt)
+    n = _elements(x, fmt)
+    _need(workspace, splitzip_workspace_bytes(n), "workspace")
     cb, cov = Codebook(), ctypes.c_double()
     fn = library().splitzip_calibrate if fmt == "bf16" else library().splitzip_calibrate_e5m2
-    _check(fn(_dev(x, "x"), x.numel(), ctypes.byref(cb), ctypes.byref(cov),
+    _check(fn(_dev(x, "x"), n, ctypes.byref(cb), ctypes.byref(cov),
               _dev(workspace, "workspace"), _stream(stream)), "splitzip_calibrate")
     return list(cb.exp), cov.value
 
@@ -227,9 +258,13 @@ def splitzip_calibrate_async(x: torch.Tensor, cb_out: torch.Tensor, covered_out:
                              workspace: torch.Tensor, fmt: str | None = None, stream=None):
     """Device-side calibration: cb_out (16 uint8) and covered_out (1 int64) on the GPU."""
     fmt = _fmt_of(x, fmt)
+    n = _elements(x, fmt)
+    _need(workspace, splitzip_workspace_bytes(n), "workspace")
+    _need(cb_out, 16, "cb_out")
+    _need(covered_out, 8, "covered_out")
     fn = (library().splitzip_calibrate_async if fmt == "bf16"
           else library().splitzip_calibrate_async_e5m2)
-    _check(fn(_dev(x, "x"), x.numel(), _dev(cb_out, "cb_out"), _dev(covered_out, "covered_out"),
+    _check(fn(_dev(x, "x"), n, _dev(cb_out, "cb_out"), _dev(covered_out, "covered_out"),
               _dev(workspace, "workspace"), _stream(stream)), "splitzip_calibrate_async")
 
 
@@ -238,10 +273,13 @@ def splitzip_histogram(x: torch.Tensor, workspace: torch.Tensor, fmt: str | None
     """Exponent histogram of x on the GPU: int64 tensor of 256 (BF16) / 32 (E5M2)
     counts; asynchronous."""
     fmt = _fmt_of(x, fmt)
+    n = _elements(x, fmt)
+    _need(workspace, splitzip_workspace_bytes(n), "workspace")
     if out is None:
         out = torch.empty(256 if fmt == "bf16" else 32, dtype=torch.int64, device=x.device)
+    _need(out, 8 * (256 if fmt == "bf16" else 32), "out")
     fn = library().splitzip_histogram if fmt == "bf16" else library().splitzip_histogram_e5m2
-    _check(fn(_dev(x, "x"), x.numel(), _dev(out, "out"), _dev(workspace, "workspace"),
+    _check(fn(_dev(x, "x"), n, _dev(out, "out"), _dev(workspace, "workspace"),
               _stream(stream)), "splitzip_histogram")
     return out
 
@@ -250,9 +288,13 @@ def splitzip_encode(x: torch.Tensor, chunk: int, codebook, streams: dict,
                     workspace: torch.Tensor, fmt: str | None = None, stream=None):
     """Enqueue one encode of x into `streams` (see alloc_streams); asynchronous."""
     fmt = _fmt_of(x, fmt)
+    n = _elements(x, fmt)
     fn = library().splitzip_encode if fmt == "bf16" else library().splitzip_encode_e5m2
+    if n and chunk > 0:
+        _need_streams(streams, n, chunk, fmt)
+        _need(workspace, splitzip_workspace_bytes(n, chunk), "workspace")
     s = _streams(streams)
-    _check(fn(_dev(x, "x"), x.numel(), chunk, ctypes.byref(_codebook(codebook)),
+    _check(fn(_dev(x, "x"), n, chunk, ctypes.byref(_codebook(codebook)),
               ctypes.byref(s), _dev(workspace, "workspace"), _stream(stream)), "splitzip_encode")
 
 
@@ -260,9 +302,13 @@ def splitzip_encode_test(x, chunk, codebook, streams, workspace, fmt=None, strea
                          spin_limit=0, flags=0):
     """splitzip_encode with the test controls of include/splitzip_testing.h."""
     fmt = _fmt_of(x, fmt)
+    n = _elements(x, fmt)
+    if n and chunk > 0:
+        _need_streams(streams, n, chunk, fmt)
+        _need(workspace, splitzip_workspace_bytes(n, chunk), "workspace")
     s, o = _streams(streams), EncodeTestOpts(spin_limit, flags)
     _check(library().splitzip_encode_test(
-        _dev(x, "x"), x.numel(), chunk, ctypes.byref(_codebook(codebook)), ctypes.byref(s),
+        _dev(x, "x"), n, chunk, ctypes.byref(_codebook(codebook)), ctypes.byref(s),
         _dev(workspace, "workspace"), _stream(stream), int(fmt == "e5m2"), ctypes.byref(o)),
         "splitzip_encode_test")
 
@@ -281,6 +327,9 @@ def splitzip_decode(streams: dict, n: int, chunk: int, codebook, y: torch.Tensor
 
     n_escapes bounds the escape entries the kernel may read (default: the
     capacity of the escape buffers)."""
+    if n > 0 and chunk > 0:
+        _need_streams(streams, n, chunk, fmt)
+        _need(y, n * _ELEM[fmt], "y")
     s = _streams(streams)
     if n_escapes is not None:
         s.esc_capacity = min(s.esc_capacity, n_escapes)
@@ -360,12 +409,14 @@ def splitzip_encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems:
     tensor `payload`.  Returns (status, payload bytes); status is OK or
     ERR_ESCAPE_OVERFLOW (payload too small: the bytes needed are returned)."""
     fmt = _fmt_of(x, fmt)
+    n = _elements(x, fmt)
     arr, k = _cbs(codebooks)
     nbytes = ctypes.c_uint64()
     sc, sh, sd = _three_streams(streams)
     st = library().splitzip_encode_to_host(
-        _ptr(x, "x"), x.numel(), FORMATS[fmt], chunk, arr, k, slice_elems, _ptr(payload, "payload"),
-        payload.numel(), ctypes.byref(nbytes), _dev(scratch, "scratch"), scratch.numel(), sc, sh, sd)
+        _ptr(x, "x"), n, FORMATS[fmt], chunk, arr, k, slice_elems, _ptr(payload, "payload"),
+        _nbytes(payload), ctypes.byref(nbytes), _dev(scratch, "scratch"), _nbytes(scratch),
+        sc, sh, sd)
     if st not in (OK, ERR_ESCAPE_OVERFLOW):
         _check(st, "splitzip_encode_to_host")
     return int(st), int(nbytes.value)
@@ -374,10 +425,18 @@ def splitzip_encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems:
 def splitzip_decode_from_host(payload: torch.Tensor, nbytes: int, y: torch.Tensor,
                               scratch: torch.Tensor, streams):
     """Decode a host payload into y (GPU or pinned host tensor); synchronous."""
+    _need(payload, nbytes, "payload")
+    if not payload.is_cuda:
+        # The library checks y's element count against the payload; its element
+        # width (which the payload's format fixes) only the tensor knows.
+        info = PayloadInfo()
+        if library().splitzip_payload_parse(_ptr(payload, "payload"), nbytes,
+                                            ctypes.byref(info), None, 0) == OK:
+            _elements(y, {v: k for k, v in FORMATS.items()}[int(info.format)], "y")
     sc, sh, sd = _three_streams(streams)
     _check(library().splitzip_decode_from_host(
         _ptr(payload, "payload"), nbytes, _ptr(y, "y"), y.numel(), _dev(scratch, "scratch"),
-        scratch.numel(), sc, sh, sd), "splitzip_decode_from_host")
+        _nbytes(scratch), sc, sh, sd), "splitzip_decode_from_host")
 
 
 def encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems: int, scratch, streams,

@@ -114,3 +114,32 @@ def test_codec_object_api():
     assert enc.n_escapes == ref["n_escapes"]
     assert enc.compressed_bytes == oracle.compressed_bytes(x.numel(), 1024, ref["n_escapes"])
     assert enc.ratio <= 4 / 3
+
+
+def test_binding_rejects_undersized_buffers():
+    """The C ABI takes plain pointers, so the Python binding checks every buffer
+    against n (and the element width against the format) before anything is
+    enqueued."""
+    ensure_library()
+    n, chunk = 100_000, 1024
+    x = torch.ones(n, dtype=torch.bfloat16, device="cuda")
+    cb = list(range(120, 136))
+    ws = sz.alloc_workspace(n, x.device)
+    st = sz.alloc_streams(n, chunk, "bf16", device=x.device)
+    small = {k: (v[: v.numel() // 2] if k in ("codes", "signman", "chunk_off") else v)
+             for k, v in st.items()}
+    bad_calls = [
+        lambda: sz.splitzip_encode(x, chunk, cb, small, ws, "bf16"),
+        lambda: sz.splitzip_encode(x, chunk, cb, st, ws[:4096], "bf16"),
+        lambda: sz.splitzip_encode(x.view(torch.uint8), chunk, cb, st, ws, "bf16"),
+        lambda: sz.splitzip_decode(st, n, chunk, cb, torch.empty(n - 1, dtype=x.dtype,
+                                                                 device=x.device), "bf16"),
+        lambda: sz.splitzip_decode(small, n, chunk, cb, torch.empty_like(x), "bf16"),
+        lambda: sz.splitzip_calibrate(x, ws[:4096], "bf16"),
+        lambda: sz.splitzip_histogram(x, ws, "bf16", out=torch.empty(8, dtype=torch.int64,
+                                                                     device=x.device)),
+    ]
+    for i, call in enumerate(bad_calls):
+        with pytest.raises(sz.SplitZipError) as err:
+            call()
+        assert err.value.status == sz.ERR_INVALID_ARG, i
