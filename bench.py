@@ -91,14 +91,23 @@ KERNEL_SOURCES = ("encode_multi.cu", "decode.cu", "common.cuh", "fields.cuh", "k
                   "lookback.cuh")
 
 
+def _code_only(src: str) -> str:
+    """C++ source without comments and whitespace: what the compiler sees."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return re.sub(r"\s+", "", src)
+
+
 def kernel_source_sha() -> str:
-    """Hash of the timed kernels' sources; a stored ncu traffic figure is used
-    only while it matches (a changed kernel makes the figure stale)."""
+    """Hash of the timed kernels' sources, comments and whitespace left out; a
+    stored ncu traffic figure is used only while it matches (a changed kernel
+    makes the figure stale, a changed comment does not)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lossless_bf16_kv_gb300", "csrc")
     for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -6,20 +6,21 @@
 // reassemble sign, exponent and mantissa, and put the raw exponent of every
 // escape back at its position; the result is bitwise identical to the input.
 //
-// One launch, no communication between CTAs and no CTA barrier.  Warps walk
-// contiguous segments (1024 BF16 or 2048 E5M2 elements) grid-stride:
-//   - the dense streams (codes, sign+mantissa) of a segment reach shared
-//     memory through a per-warp ring of kDecodeStages slots filled by cp.async
-//     (16 bytes per lane per copy, fully coalesced), kDecodeStages - 1
-//     segments ahead of the one being decoded;
+// One launch, no communication between CTAs; the only CTA barrier follows the
+// BF16 table build at the start.  Warps walk contiguous segments (1024 BF16
+// or 2048 E5M2 elements) grid-stride:
+//   - the dense streams (codes, sign+mantissa) of the next segment are loaded
+//     into registers (BF16), or reach shared memory through a per-warp ring of
+//     kDecodeStages slots filled by cp.async (E5M2: 16 bytes per lane per
+//     copy, fully coalesced, kDecodeStages - 1 segments ahead);
 //   - the segment's slice [lo, hi) of the escape stream is found two segments
 //     ahead (chunk_off at a chunk start, else a warp-wide search of the
 //     ascending positions inside the chunk) and its first 32 escapes are
 //     loaded one segment ahead;
 //   - each lane decodes its exponents in registers: BF16 two codes at a time
 //     from a 256-entry shared-memory table of code bytes (built per CTA from
-//     the codebook), E5M2 four at a time by byte permutes of the 16 entries
-//     held in four registers;
+//     the codebook), E5M2 a code word (eight codes) at a time by byte permutes
+//     of the 16 entries held in four registers;
 //   - a segment with escapes parks its exponent words in shared memory, each
 //     lane holding an escape overwrites that element's exponent byte, and the
 //     words are read back (escapes beyond the first 32 of a segment are read
