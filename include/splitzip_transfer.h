@@ -149,6 +149,29 @@ splitzip_status splitzip_encode_to_host(const void* x, uint64_t n, uint32_t form
                                         size_t scratch_bytes, splitzip_stream_t s_compute,
                                         splitzip_stream_t s_h2d, splitzip_stream_t s_d2h);
 
+/* A CUDA event (a cudaEvent_t). */
+typedef struct CUevent_st *splitzip_event_t;
+
+/* splitzip_encode_to_host for a tensor still being written slice by slice (a
+ * KV cache produced layer by layer, the pages' producer side of the transfer
+ * path): before the call reads slice i -- its host-to-device copy or its
+ * encode -- the call's streams wait on slice_ready[i], an event the producer
+ * records once slice i is written.  Slices whose events have completed are
+ * encoded and copied out while later slices are still being produced.
+ * num_events: 0 (slice_ready may then be NULL; the call is exactly
+ * splitzip_encode_to_host) or the number of slices, ceil(n / slice_elems).
+ * The events are only waited on, never recorded or destroyed.  Other
+ * arguments, errors and the payload as for splitzip_encode_to_host. */
+splitzip_status splitzip_encode_to_host_events(const void* x, uint64_t n, uint32_t format,
+                                               uint32_t chunk_size, const splitzip_codebook* cbs,
+                                               uint32_t num_cbs, uint64_t slice_elems,
+                                               void* h_payload, uint64_t payload_capacity,
+                                               uint64_t* payload_bytes, void* d_scratch,
+                                               size_t scratch_bytes, splitzip_stream_t s_compute,
+                                               splitzip_stream_t s_h2d, splitzip_stream_t s_d2h,
+                                               const splitzip_event_t* slice_ready,
+                                               uint32_t num_events);
+
 /* Decode a host payload (as written by splitzip_encode_to_host, `bytes` long,
  * in host memory, else SPLITZIP_ERR_INVALID_ARG) into y: n elements of the payload's format, in device memory or in host
  * memory (pinned for speed), 16-byte aligned.  The payload is validated with

@@ -279,6 +279,20 @@ splitzip_status splitzip_encode_to_host(const void* x, uint64_t n, uint32_t form
                                         uint64_t* payload_bytes, void* d_scratch,
                                         size_t scratch_bytes, splitzip_stream_t s_compute,
                                         splitzip_stream_t s_h2d, splitzip_stream_t s_d2h) {
+    return splitzip_encode_to_host_events(x, n, format, chunk_size, cbs, num_cbs, slice_elems,
+                                          h_payload, payload_capacity, payload_bytes, d_scratch,
+                                          scratch_bytes, s_compute, s_h2d, s_d2h, nullptr, 0);
+}
+
+splitzip_status splitzip_encode_to_host_events(const void* x, uint64_t n, uint32_t format,
+                                               uint32_t chunk_size, const splitzip_codebook* cbs,
+                                               uint32_t num_cbs, uint64_t slice_elems,
+                                               void* h_payload, uint64_t payload_capacity,
+                                               uint64_t* payload_bytes, void* d_scratch,
+                                               size_t scratch_bytes, splitzip_stream_t s_compute,
+                                               splitzip_stream_t s_h2d, splitzip_stream_t s_d2h,
+                                               const splitzip_event_t* slice_ready,
+                                               uint32_t num_events) {
     splitzip::TraceRange trace("splitzip_encode_to_host");
     if (!x || !cbs || !h_payload || !payload_bytes || !d_scratch) return SPLITZIP_ERR_INVALID_ARG;
     if (!format_ok(format) || !chunk_ok(chunk_size) || n == 0 || n > SPLITZIP_MAX_ELEMENTS)
@@ -287,6 +301,7 @@ splitzip_status splitzip_encode_to_host(const void* x, uint64_t n, uint32_t form
         return SPLITZIP_ERR_INVALID_ARG;
     const uint32_t S = (uint32_t)ceil_div(n, slice_elems);
     if (num_cbs != 1 && num_cbs != S) return SPLITZIP_ERR_INVALID_ARG;
+    if (num_events != 0 && (num_events != S || !slice_ready)) return SPLITZIP_ERR_INVALID_ARG;
     for (uint32_t i = 0; i < num_cbs; i++)
         if (!codebook_ok(cbs[i], format)) return SPLITZIP_ERR_INVALID_ARG;
     if (((uintptr_t)x & 15) || ((uintptr_t)d_scratch & 255)) return SPLITZIP_ERR_INVALID_ARG;
@@ -386,6 +401,10 @@ splitzip_status splitzip_encode_to_host(const void* x, uint64_t n, uint32_t form
         const uint8_t* src = static_cast<const uint8_t*>(x) + (uint64_t)i * slice_elems * eb;
         cudaError_t e = cudaSuccess;
         if (i >= (uint32_t)kBuffers) e = cudaStreamWaitEvent(sc, d2h_done[b], 0);  // streams of b free
+        if (e == cudaSuccess && num_events) {  // slice i has been written by its producer
+            e = cudaStreamWaitEvent(sc, (cudaEvent_t)slice_ready[i], 0);
+            if (e == cudaSuccess && host_in) e = cudaStreamWaitEvent(sh, (cudaEvent_t)slice_ready[i], 0);
+        }
         if (host_in) {
             if (e == cudaSuccess && i >= (uint32_t)kBuffers) e = cudaStreamWaitEvent(sh, enc_done[b], 0);
             if (e == cudaSuccess) e = cudaMemcpyAsync(B.raw, src, ni * eb, cudaMemcpyHostToDevice, sh);

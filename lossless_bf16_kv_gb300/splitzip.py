@@ -113,6 +113,9 @@ def library() -> ctypes.CDLL:
         "splitzip_transfer_scratch_bytes": (ctypes.c_size_t, [u32, u64, u32]),
         "splitzip_encode_to_host": (st, [vp, u64, u32, u32, cbp, u32, u64, vp, u64,
                                          ctypes.POINTER(u64), vp, ctypes.c_size_t, vp, vp, vp]),
+        "splitzip_encode_to_host_events": (st, [vp, u64, u32, u32, cbp, u32, u64, vp, u64,
+                                                ctypes.POINTER(u64), vp, ctypes.c_size_t,
+                                                vp, vp, vp, ctypes.POINTER(vp), u32]),
         "splitzip_decode_from_host": (st, [vp, u64, vp, u64, vp, ctypes.c_size_t, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -402,21 +405,37 @@ def _three_streams(streams):
     return [ctypes.c_void_p(s.cuda_stream) for s in streams]
 
 
+def _events(ready_events):
+    """A C array of the events' cudaEvent_t handles (None for no events)."""
+    if not ready_events:
+        return None, 0
+    arr = (ctypes.c_void_p * len(ready_events))()
+    for i, ev in enumerate(ready_events):
+        h = ev.cuda_event
+        if not h:   # a torch event is created lazily, on its first record
+            raise ValueError(f"ready event {i} has not been recorded")
+        arr[i] = h
+    return arr, len(ready_events)
+
+
 def splitzip_encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems: int,
                             payload: torch.Tensor, scratch: torch.Tensor, streams,
-                            fmt: str | None = None):
+                            fmt: str | None = None, ready_events=None):
     """Encode x (GPU or pinned host tensor) slice by slice into the host uint8
     tensor `payload`.  Returns (status, payload bytes); status is OK or
-    ERR_ESCAPE_OVERFLOW (payload too small: the bytes needed are returned)."""
+    ERR_ESCAPE_OVERFLOW (payload too small: the bytes needed are returned).
+    ready_events: None, or one recorded torch.cuda.Event per slice; slice i is
+    read only after its event completes (a tensor still being produced)."""
     fmt = _fmt_of(x, fmt)
     n = _elements(x, fmt)
     arr, k = _cbs(codebooks)
+    evs, ne = _events(ready_events)
     nbytes = ctypes.c_uint64()
     sc, sh, sd = _three_streams(streams)
-    st = library().splitzip_encode_to_host(
+    st = library().splitzip_encode_to_host_events(
         _ptr(x, "x"), n, FORMATS[fmt], chunk, arr, k, slice_elems, _ptr(payload, "payload"),
         _nbytes(payload), ctypes.byref(nbytes), _dev(scratch, "scratch"), _nbytes(scratch),
-        sc, sh, sd)
+        sc, sh, sd, evs, ne)
     if st not in (OK, ERR_ESCAPE_OVERFLOW):
         _check(st, "splitzip_encode_to_host")
     return int(st), int(nbytes.value)
@@ -440,7 +459,8 @@ def splitzip_decode_from_host(payload: torch.Tensor, nbytes: int, y: torch.Tenso
 
 
 def encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems: int, scratch, streams,
-                   fmt: str | None = None, payload: torch.Tensor | None = None):
+                   fmt: str | None = None, payload: torch.Tensor | None = None,
+                   ready_events=None):
     """splitzip_encode_to_host into a pinned payload, grown once if too small.
     Returns (payload tensor, payload bytes)."""
     fmt = _fmt_of(x, fmt)
@@ -449,11 +469,11 @@ def encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems: int, scr
         cap = splitzip_payload_bytes_bound(n, chunk, slice_elems, n // 128 + 4096, fmt)
         payload = torch.empty(cap, dtype=torch.uint8).pin_memory()
     st, nbytes = splitzip_encode_to_host(x, chunk, codebooks, slice_elems, payload, scratch,
-                                         streams, fmt)
+                                         streams, fmt, ready_events)
     if st == ERR_ESCAPE_OVERFLOW:
         payload = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
         st, nbytes = splitzip_encode_to_host(x, chunk, codebooks, slice_elems, payload, scratch,
-                                             streams, fmt)
+                                             streams, fmt, ready_events)
         _check(st, "splitzip_encode_to_host")
     return payload, nbytes
 

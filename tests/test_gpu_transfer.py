@@ -150,3 +150,64 @@ def test_payload_must_be_host_memory():
     with pytest.raises(sz.SplitZipError) as err:
         sz.splitzip_decode_from_host(on_device, nbytes, torch.empty_like(x), scratch, streams)
     assert err.value.status == sz.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+@pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
+def test_encode_waits_for_each_slice_to_be_produced(fmt, where):
+    """A producer on its own stream writes the tensor slice by slice, each slice
+    after a spin of several milliseconds, and records one event per slice; the
+    encode call is issued at once.  Every slice must be read only after its
+    event: the payload equals the oracle's payload of the produced data, not of
+    the zeros the buffer held when the call was made."""
+    ensure_library()
+    chunk, se = 1024, 1 << 17
+    src = _kv(fmt, 4 * se + 3 * chunk + 9, seed=11)     # five slices, the last ragged
+    n = src.numel()
+    cb = [int(c) for c in oracle.calibrate(host_bits(src), fmt)[0]]
+    x = (torch.zeros_like(src) if where == "device"
+         else torch.zeros(src.shape, dtype=src.dtype).pin_memory())
+    scratch, streams = sz.alloc_transfer_scratch(se, chunk, fmt), _streams()
+    torch.cuda.synchronize()
+    producer = torch.cuda.Stream()
+    events = []
+    with torch.cuda.stream(producer):
+        for lo in range(0, n, se):
+            torch.cuda._sleep(10_000_000)                # about 5 ms at 2 GHz
+            x[lo:lo + se].copy_(src[lo:lo + se], non_blocking=True)
+            events.append(torch.cuda.Event())
+            events[-1].record(producer)
+    payload, nbytes = sz.encode_to_host(x, chunk, cb, se, scratch, streams, fmt,
+                                        ready_events=events)
+    bits = host_bits(src)
+    assert payload[:nbytes].numpy().tobytes() == op.write(bits, fmt, chunk, se, cb)
+    y = torch.empty_like(src)
+    sz.splitzip_decode_from_host(payload, nbytes, y, scratch, streams)
+    assert np.array_equal(host_bits(y), bits)
+
+
+def test_ready_events_are_checked():
+    """One event per slice or none: other counts, and events never recorded,
+    are rejected before any work is enqueued."""
+    ensure_library()
+    fmt, chunk, se = "bf16", 1024, 1 << 16
+    x = _kv(fmt, 3 * se, seed=12)
+    cb = [int(c) for c in oracle.calibrate(host_bits(x), fmt)[0]]
+    scratch, streams = sz.alloc_transfer_scratch(se, chunk, fmt), _streams()
+    payload = torch.empty(sz.splitzip_payload_bytes_bound(x.numel(), chunk, se, x.numel(), fmt),
+                          dtype=torch.uint8).pin_memory()
+    events = [torch.cuda.Event() for _ in range(4)]
+    for ev in events:
+        ev.record()
+    for evs in (events[:2], events):                     # three slices
+        with pytest.raises(sz.SplitZipError) as err:
+            sz.splitzip_encode_to_host(x, chunk, cb, se, payload, scratch, streams, fmt,
+                                       ready_events=evs)
+        assert err.value.status == sz.ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        sz.splitzip_encode_to_host(x, chunk, cb, se, payload, scratch, streams, fmt,
+                                   ready_events=[torch.cuda.Event()] * 3)
+    st, nbytes = sz.splitzip_encode_to_host(x, chunk, cb, se, payload, scratch, streams, fmt,
+                                            ready_events=events[:3])
+    assert st == sz.OK
+    assert payload[:nbytes].numpy().tobytes() == op.write(host_bits(x), fmt, chunk, se, cb)
