@@ -209,6 +209,34 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
+// An L2 policy that marks lines evict-last (for small data that a following
+// kernel reads back while large streams pass through L2).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// Stores under an L2 cache policy.
+__device__ __forceinline__ void st_policy2(void* p, uint16_t v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p), "h"(v), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void st_policy8(void* p, uint2 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "l"(pol)
+                 : "memory");
+}
+// Drops the 128-byte L2 line at p (128-byte aligned) without writing it back:
+// its contents become undefined.  For scratch lines no one reads again.
+__device__ __forceinline__ void discard_l2_line(void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+// Loads of data read for the last time (evict-first in L2).
+__device__ __forceinline__ uint16_t ld_last2(const void* p) {
+    uint16_t v;
+    asm volatile("ld.global.lu.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
 // cp_async16 with an L2 cache policy for the global read.
 __device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t pol) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),

@@ -55,6 +55,20 @@ struct MultiPtrs {
     uint16_t* seg_ent;
 };
 
+// Stores of segment counts and escape list entries: under the L2 policy pol
+// (evict-last) for a format whose lists stay in L2 until placement, plain
+// otherwise.
+template <bool kKeep>
+__device__ __forceinline__ void st_list2(uint16_t* p, uint32_t v, uint64_t pol) {
+    if constexpr (kKeep) st_policy2(p, (uint16_t)v, pol);
+    else *p = (uint16_t)v;
+}
+template <bool kKeep>
+__device__ __forceinline__ void st_list8(uint16_t* p, uint2 v, uint64_t pol) {
+    if constexpr (kKeep) st_policy8(p, v, pol);
+    else *reinterpret_cast<uint2*>(p) = v;
+}
+
 // Warp-wide exclusive scan of one word per lane, excl = sum of p over the
 // lower lanes.  Also returns lane 31's exclusive prefix and word, from which
 // the caller forms the warp totals (the formats pack several small counts in
@@ -93,6 +107,10 @@ struct Bf16Dense {
     static constexpr int kSegs = 32;
     static constexpr int kSegLen = 256;
     static constexpr int kOffBits = 8;
+    static constexpr int kPlaceRounds = 4;  // placement: tiles per warp, one per round
+    static constexpr int kPreload = 4;      // placement: entries per segment loaded ahead
+    // Counts and lists stored plainly: evict-last stores measured 3% slower here.
+    static constexpr bool kKeepLists = false;
     static constexpr uint32_t kExpMask = 0xFFu;
     struct Tables {
         uint32_t t[4][256];
@@ -236,38 +254,41 @@ struct Bf16Dense {
     // number of lower lanes whose same group has an escape, a segment's total
     // the population of that ballot.
     static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
-                                                           uint16_t* ent, const uint8_t* in) {
+                                                           uint16_t* ent, const uint8_t* in,
+                                                           uint64_t pol) {
         const uint32_t lane = threadIdx.x & 31, lt = (1u << lane) - 1u;
         uint32_t has[kGroups];
 #pragma unroll
         for (int k = 0; k < kGroups; k++) has[k] = __ballot_sync(0xFFFFFFFFu, kp.miss[k] != 0);
         const uint32_t c0 = __popc(has[0]), c1 = __popc(has[1]), c2 = __popc(has[2]);
         if (lane == 0)
-            *reinterpret_cast<uint2*>(row + slot(0)) =
-                make_uint2(c0 | (c1 << 16), c2 | (__popc(has[3]) << 16));
+            st_list8<kKeepLists>(row + slot(0),
+                                 make_uint2(c0 | (c1 << 16), c2 | (__popc(has[3]) << 16)), pol);
         if (kp.cnt) {
             uint32_t excl = 0;
 #pragma unroll
             for (int k = 0; k < kGroups; k++) excl |= (uint32_t)__popc(has[k] & lt) << (8 * k);
             const uint32_t base[kGroups] = {0u, c0, c0 + c1, c0 + c1 + c2};
-            emit(kp, excl, base, ent, in);
+            emit(kp, excl, base, ent, in, pol);
         }
     }
     // Counts and escapes in general: one packed warp scan of the four groups'
     // counts.
     static __device__ __forceinline__ void bookkeep_multi(const Keep& kp, uint16_t* row,
-                                                          uint16_t* ent, const uint8_t* in) {
+                                                          uint16_t* ent, const uint8_t* in,
+                                                          uint64_t pol) {
         uint32_t excl, e31, p31;
         warp_scan_excl(kp.cnt, excl, e31, p31);
         const uint32_t t02 = (e31 & 0x00FF00FFu) + (p31 & 0x00FF00FFu);  // totals of groups 0, 2
         const uint32_t t13 = ((e31 >> 8) & 0x00FF00FFu) + ((p31 >> 8) & 0x00FF00FFu);  // 1, 3
         if ((threadIdx.x & 31) == 0)
-            *reinterpret_cast<uint2*>(row + slot(0)) =
-                make_uint2(__byte_perm(t02, t13, 0x5410), __byte_perm(t02, t13, 0x7632));
+            st_list8<kKeepLists>(
+                row + slot(0),
+                make_uint2(__byte_perm(t02, t13, 0x5410), __byte_perm(t02, t13, 0x7632)), pol);
         if (kp.cnt) {
             const uint32_t c0 = t02 & 0xFFFFu, c1 = t13 & 0xFFFFu, c2 = t02 >> 16;
             const uint32_t base[kGroups] = {0u, c0, c0 + c1, c0 + c1 + c2};
-            emit(kp, excl, base, ent, in);
+            emit(kp, excl, base, ent, in, pol);
         }
     }
 
@@ -276,7 +297,7 @@ struct Bf16Dense {
     // bases; in: the tile's input (group k of this thread at element loff(k)).
     static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl,
                                                 const uint32_t (&base)[kGroups], uint16_t* ent,
-                                                const uint8_t* in) {
+                                                const uint8_t* in, uint64_t pol) {
         const uint32_t lane = threadIdx.x & 31;
         uint16_t* e = ent + (threadIdx.x >> 5) * kWarpCap;
 #pragma unroll
@@ -290,7 +311,7 @@ struct Bf16Dense {
                 m &= m - 1;
                 const uint32_t j = (b & 3u) + ((b >> 4) << 2);
                 const uint32_t ex = ((uint32_t)x[j] >> 7) & kExpMask;
-                e[g++] = (uint16_t)((8 * lane + j) | (ex << kOffBits));
+                st_list2<kKeepLists>(e + g++, (8 * lane + j) | (ex << kOffBits), pol);
             }
         }
     }
@@ -321,13 +342,21 @@ struct E5m2Dense {
     static constexpr int kSegs = kWarps;              // 8
     static constexpr int kSegLen = 1024;
     static constexpr int kOffBits = 10;
+    static constexpr int kPlaceRounds = 2;  // placement: rounds of four tiles per warp
+    static constexpr int kPreload = 8;      // placement: entries per segment loaded ahead
+    // Counts and lists stored evict-last, so that placement finds them in L2.
+    static constexpr bool kKeepLists = true;
     static constexpr uint32_t kExpMask = 0x1Fu;
-    // Code table indexed by the raw byte with its sign bit cleared (exponent
-    // in bits 2..6, mantissa in bits 0..1): entry = code, or kMissEntry for an
-    // exponent outside the codebook.  The four bytes of one exponent share a
-    // word, so lanes with different exponents always read different banks.
+    // Eight code tables, one per element position q = 0..7 within a pair of
+    // input words, indexed by exponent.  Entry t[q][e] holds e's code shifted
+    // to nibble q & 3 (bits 0..15: the codes of one word's four elements) and,
+    // for an exponent outside the codebook, code 0 with a flag at bit 16 + q.
+    // OR-ing a word's four entries gives its 16 code bits; OR-ing a pair's two
+    // results gives the pair's 8 escape flags in byte 2.  A byte masked with
+    // 0x7C is 4e, the entry's byte offset within its table: lanes reading one
+    // table with different exponents always hit different banks.
     struct Tables {
-        uint8_t t[128];
+        uint32_t t[8][32];
     };
     static constexpr int kElemBytes = 1;
     static constexpr int kMinBlocks = 6;  // resident CTAs per SM (registers cap it at 40 each)
@@ -336,25 +365,25 @@ struct E5m2Dense {
         uint32_t cnt;  // popcount of mm
     };
     static __device__ __forceinline__ void build_tables(Tables& tb, const uint32_t (&cbw)[4]) {
-        const uint32_t tid = threadIdx.x;
-        if (tid < 128) {
-            const uint32_t e = tid >> 2;
-            uint32_t ent = kMissEntry;
+        static_assert(kThreads == 256, "one table entry per thread");
+        const uint32_t q = threadIdx.x >> 5, e = threadIdx.x & 31;
+        uint32_t ent = 1u << (16 + q);
 #pragma unroll
-            for (int k = 0; k < 16; k++)  // codebook entries are distinct
-                if (((cbw[k >> 2] >> (8 * (k & 3))) & 0xFFu) == e) ent = (uint32_t)k;
-            tb.t[tid] = (uint8_t)ent;
-        }
+        for (int k = 0; k < 16; k++)  // codebook entries are distinct
+            if (((cbw[k >> 2] >> (8 * (k & 3))) & 0xFFu) == e) ent = (uint32_t)k << (4 * (q & 3));
+        tb.t[q][e] = ent;
         __syncthreads();
     }
-    // Entries of the four bytes of w, one per byte.
-    static __device__ __forceinline__ uint32_t lookup_raw4(const uint8_t* t, uint32_t w) {
-        const uint32_t m = w & 0x7F7F7F7Fu;
-        const uint32_t e0 = t[__byte_perm(m, 0u, 0x4440)];
-        const uint32_t e1 = t[__byte_perm(m, 0u, 0x4441)];
-        const uint32_t e2 = t[__byte_perm(m, 0u, 0x4442)];
-        const uint32_t e3 = t[__byte_perm(m, 0u, 0x4443)];
-        return __byte_perm(__byte_perm(e0, e1, 0x0040), __byte_perm(e2, e3, 0x0040), 0x5410);
+    // Table entries of the four bytes of w, OR-ed: table q0 + b for byte b.
+    template <int q0>
+    static __device__ __forceinline__ uint32_t lookup_word(const Tables& tb, uint32_t w) {
+        const uint32_t m = w & 0x7C7C7C7Cu;  // 4 x exponent in each byte
+        const char* t = reinterpret_cast<const char*>(&tb.t[q0][0]);
+        auto at = [&](int b, uint32_t off) {
+            return *reinterpret_cast<const uint32_t*>(t + 128 * b + off);
+        };
+        return at(0, __byte_perm(m, 0u, 0x4440)) | at(1, __byte_perm(m, 0u, 0x4441)) |
+               at(2, __byte_perm(m, 0u, 0x4442)) | at(3, __byte_perm(m, 0u, 0x4443));
     }
     static __device__ __forceinline__ uint32_t slot(int) { return threadIdx.x >> 5; }
     static __device__ __forceinline__ uint32_t storage(uint32_t s) { return s; }
@@ -377,7 +406,7 @@ struct E5m2Dense {
         const uint32_t base = 64 * (threadIdx.x >> 5) + 2 * (threadIdx.x & 31);
         const uint4 v0 = stage[base], v1 = stage[base + 1];
         const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        finish(a, tb.t, t0 + threadIdx.x * 32, w, true, kp);
+        finish(a, tb, t0 + threadIdx.x * 32, w, true, kp);
     }
     static __device__ __forceinline__ void process_partial(const EncodeArgs& a, const Tables& tb,
                                                            uint32_t t0, Keep& kp) {
@@ -406,32 +435,29 @@ struct E5m2Dense {
                 w[m] = acc;
             }
         }
-        finish(a, tb.t, i, w, whole, kp);
+        finish(a, tb, i, w, whole, kp);
     }
 
     // Fields, codes and stores of the 32 elements at i (input words w).
-    static __device__ __forceinline__ void finish(const EncodeArgs& a, const uint8_t* table,
+    static __device__ __forceinline__ void finish(const EncodeArgs& a, const Tables& tb,
                                                   uint32_t i, const uint32_t (&w)[8], bool whole,
                                                   Keep& kp) {
-        uint32_t f12[8], ent[8];
+        uint32_t f12[8], r[8];
 #pragma unroll
         for (int m = 0; m < 8; m++) f12[m] = fields12_e5m2(w[m]);
 #pragma unroll
-        for (int m = 0; m < 8; m++) ent[m] = lookup_raw4(table, w[m]);
-        uint4 codes;
-        codes.x = pack_nibbles(ent[0], ent[1]);
-        codes.y = pack_nibbles(ent[2], ent[3]);
-        codes.z = pack_nibbles(ent[4], ent[5]);
-        codes.w = pack_nibbles(ent[6], ent[7]);
-        // Escape flags (bit 4 of each entry byte, at bits 4, 12, 20, 28) to
-        // bits 4m..4m+3: multiplying by 2^0 + 2^7 + 2^14 + 2^21 moves flag b
-        // to bit 25 + b; every other partial product lands below bit 25.
-        kp.mm = 0;
-#pragma unroll
-        for (int m = 0; m < 8; m++) {
-            const uint32_t nib = ((ent[m] & 0x10101010u) * 0x00204081u) >> 25;
-            kp.mm |= nib << (4 * m);
+        for (int m = 0; m < 8; m += 2) {
+            r[m] = lookup_word<0>(tb, w[m]);
+            r[m + 1] = lookup_word<4>(tb, w[m + 1]);
         }
+        uint4 codes;  // word p: the codes of words 2p (low half) and 2p + 1
+        codes.x = __byte_perm(r[0], r[1], 0x5410);
+        codes.y = __byte_perm(r[2], r[3], 0x5410);
+        codes.z = __byte_perm(r[4], r[5], 0x5410);
+        codes.w = __byte_perm(r[6], r[7], 0x5410);
+        // Byte 2 of r[2p] | r[2p + 1]: the flags of elements 8p..8p+7, in order.
+        const uint32_t o0 = r[0] | r[1], o1 = r[2] | r[3], o2 = r[4] | r[5], o3 = r[6] | r[7];
+        kp.mm = __byte_perm(__byte_perm(o0, o1, 0x0062), __byte_perm(o2, o3, 0x0062), 0x5410);
         kp.cnt = __popc(kp.mm);
         // 8 x 12 bits -> 96 bits, little-endian.
         const uint32_t s0 = f12[0] | (f12[1] << 12) | (f12[2] << 24);
@@ -457,19 +483,21 @@ struct E5m2Dense {
     static __device__ __forceinline__ bool multi(const Keep& kp) { return kp.cnt >= 2; }
     // Counts and escapes when no lane of the warp holds more than one escape.
     static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
-                                                           uint16_t* ent, const uint8_t* in) {
+                                                           uint16_t* ent, const uint8_t* in,
+                                                           uint64_t pol) {
         const uint32_t lane = threadIdx.x & 31;
         const uint32_t has = __ballot_sync(0xFFFFFFFFu, kp.cnt != 0);
-        if (lane == 0) row[slot(0)] = (uint16_t)__popc(has);
-        if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent, in);
+        if (lane == 0) st_list2<kKeepLists>(row + slot(0), __popc(has), pol);
+        if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent, in, pol);
     }
 
     static __device__ __forceinline__ void bookkeep_multi(const Keep& kp, uint16_t* row,
-                                                          uint16_t* ent, const uint8_t* in) {
+                                                          uint16_t* ent, const uint8_t* in,
+                                                          uint64_t pol) {
         uint32_t excl, e31, p31;
         warp_scan_excl(kp.cnt, excl, e31, p31);
-        if ((threadIdx.x & 31) == 0) row[slot(0)] = (uint16_t)(e31 + p31);
-        if (kp.cnt) emit(kp, excl, ent, in);
+        if ((threadIdx.x & 31) == 0) st_list2<kKeepLists>(row + slot(0), e31 + p31, pol);
+        if (kp.cnt) emit(kp, excl, ent, in, pol);
     }
     // One segment per warp: segment s's entries are warp s's whole list.
     static __device__ __forceinline__ uint32_t seg_list(uint32_t s) { return s; }
@@ -478,14 +506,15 @@ struct E5m2Dense {
     // The lane's first escapes, from rank excl on, into the segment's entries;
     // in: the tile's input (this lane's 32 elements at byte 32 t).
     static __device__ __forceinline__ void emit(const Keep& kp, uint32_t excl, uint16_t* ent,
-                                                const uint8_t* in) {
+                                                const uint8_t* in, uint64_t pol) {
         const uint32_t lane = threadIdx.x & 31;
         const uint8_t* x = in + 32 * threadIdx.x;
         uint16_t* e = ent + slot(0) * kWarpCap;
         uint32_t g = excl;
         for (uint32_t m = kp.mm; m && g < (uint32_t)kWarpCap; m &= m - 1) {
             const uint32_t j = __ffs(m) - 1;
-            e[g++] = (uint16_t)((32 * lane + j) | ((((uint32_t)x[j] >> 2) & kExpMask) << kOffBits));
+            st_list2<kKeepLists>(
+                e + g++, (32 * lane + j) | ((((uint32_t)x[j] >> 2) & kExpMask) << kOffBits), pol);
         }
     }
 
@@ -518,6 +547,9 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
     extern __shared__ uint4 ring[];  // [S][L][kThreads]
     __shared__ typename F::Tables tables;
     F::build_tables(tables, a.cbw);
+    // With F::kKeepLists, counts and list entries stay in L2 for the prefix and
+    // placement passes while the tensor streams through.
+    const uint64_t keep = F::kKeepLists ? l2_evict_last_policy() : 0u;
     const uint32_t full_tiles = a.n / (uint32_t)kTileElems;
     auto fill = [&](uint32_t tile, int slot) {
         if (tile < full_tiles) {
@@ -548,9 +580,9 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
         uint16_t* row = p.seg_cnt + (size_t)tile * kSegsMax;
         uint16_t* ent = p.seg_ent + (size_t)tile * kEntries;
         if (!__any_sync(0xFFFFFFFFu, F::multi(kp))) {
-            F::bookkeep_single(kp, row, ent, in);
+            F::bookkeep_single(kp, row, ent, in, keep);
         } else {
-            F::bookkeep_multi(kp, row, ent, in);
+            F::bookkeep_multi(kp, row, ent, in, keep);
         }
         if (F::kSharedStage) __syncwarp();  // every lane has read the stage before the refill
         fill(tile + S * gridDim.x, slot);
@@ -581,9 +613,9 @@ __device__ void prefix_finished(const EncodeArgs& a, uint32_t epoch) {
     }
 }
 
+template <int SEGS>
 __global__ void __launch_bounds__(kThreads) prefix_kernel(const EncodeArgs a, const MultiPtrs p,
-                                                          uint32_t num_tiles, uint32_t num_blocks,
-                                                          uint32_t segs) {
+                                                          uint32_t num_tiles, uint32_t num_blocks) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     __shared__ uint32_t s_blk, s_epoch, s_excl;
     __shared__ uint32_t s_warp[kWarps];
@@ -601,8 +633,9 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const EncodeArgs a, co
         }
         return;
     }
-    // Tile totals: the sum of each tile's segment counts (16-bit, 32 per tile,
-    // the first `segs` in use).
+    // Tile totals: the sum of each tile's segment counts (16-bit, 32 slots per
+    // tile, the first SEGS in use).  The row count is a constant, so all of a
+    // thread's row loads are issued before the first is summed.
     const uint32_t base = blk * (uint32_t)kScanTiles + tid * 8;
     uint32_t v[8];
 #pragma unroll
@@ -610,9 +643,9 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const EncodeArgs a, co
         v[i] = 0;
         if (base + i >= num_tiles) continue;
         const uint4* row = reinterpret_cast<const uint4*>(p.seg_cnt + (size_t)(base + i) * kSegsMax);
+        static_assert(SEGS % 8 == 0 && SEGS <= kSegsMax, "whole 16-byte rows of counts");
 #pragma unroll
-        for (int q = 0; q < kSegsMax / 8; q++) {
-            if ((uint32_t)q * 8 >= segs) break;
+        for (int q = 0; q < SEGS / 8; q++) {
             const uint4 c = row[q];
             const uint32_t w = (c.x & 0xFFFFu) + (c.x >> 16) + (c.y & 0xFFFFu) + (c.y >> 16) +
                                (c.z & 0xFFFFu) + (c.z >> 16) + (c.w & 0xFFFFu) + (c.w >> 16);
@@ -683,50 +716,98 @@ __device__ __forceinline__ bool in_codebook(const uint32_t (&cbw)[4], uint32_t e
     return z != 0;
 }
 
-// A warp places the escapes of 32 / kSegs consecutive tiles (BF16: one, E5M2:
-// four), lane l taking segment l mod kSegs (element order) of tile l / kSegs.
+// A warp places the escapes of F::kPlaceRounds x 32 / kSegs consecutive tiles
+// (BF16: 4 x 1, E5M2: 2 x 4): in round r lane l takes segment l mod kSegs
+// (element order) of tile tile0 + r * 32 / kSegs + l / kSegs.  Every round's
+// tile offset and counts are loaded before any is used, and every round's
+// first F::kPreload entries before any escape is stored (loads cannot pass
+// the stores, which the compiler must assume may alias them), so a warp waits
+// for two memory round trips in all rather than two per tile.
 template <class F>
-__global__ void __launch_bounds__(kThreads, 8) place_kernel(const EncodeArgs a, const MultiPtrs p,
+__global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, const MultiPtrs p,
                                                             uint32_t num_tiles) {
     constexpr uint32_t kOffMask = (1u << F::kOffBits) - 1u;
     constexpr uint32_t SEGS = F::kSegs, TPW = 32 / F::kSegs;
+    constexpr int R = F::kPlaceRounds, K = F::kPreload;
     const uint32_t cbw[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW;
+    const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW * R;
     if (tile0 >= num_tiles) return;  // warp-uniform
     const uint32_t sub = lane / SEGS, sgl = lane % SEGS;  // this lane's tile and segment
-    const uint32_t tile = tile0 + sub;
-    const bool tvalid = tile < num_tiles;
-    const uint32_t t0 = tile * (uint32_t)kTileElems;
-    const uint32_t len = !tvalid ? 0u : a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
-    const uint32_t q0 = chunk_quot32(a.cdiv, t0), r0 = t0 - q0 * a.cdiv.d;
-    const uint32_t excl = tvalid ? p.tile_excl[tile] : 0u;
-    const uint32_t cnt = tvalid ? p.seg_cnt[(size_t)tile * kSegsMax + F::storage(sgl)] : 0u;
-    // Exclusive scan of the counts within each tile's group of SEGS lanes.
-    uint32_t incl = cnt;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= (uint32_t)d) incl += u;
-    }
-    const uint32_t first = __shfl_sync(0xFFFFFFFFu, incl - cnt, lane & ~(SEGS - 1));
-    const uint32_t off = incl - cnt - first;
-    const uint16_t* ent = p.seg_ent + (size_t)tile * kEntries;
-    // Where this lane's segment's entries start in its warp list.
-    const uint32_t sbase = F::seg_base(sgl, cnt, lane & ~(SEGS - 1));
+    const uint32_t lbase = lane & ~(SEGS - 1);
+    const uint32_t s0 = sgl * F::kSegLen;  // the segment's tile-local start
+    auto tile_of = [&](int r) { return tile0 + (uint32_t)r * TPW + sub; };
 
-    // Escapes of segment sgl of this lane's tile, in element order.
-    if (cnt) {
-        const uint32_t s0 = sgl * F::kSegLen;
-        const uint32_t g0 = excl + off;
-        if (sbase + cnt <= (uint32_t)kWarpCap) {
-            for (uint32_t r = 0; r < cnt; r++) {
-                const uint32_t e = ent[F::seg_list(sgl) * kWarpCap + sbase + r];
-                const uint32_t x = r0 + s0 + (e & kOffMask);
-                put_escape(a, g0 + r, x - chunk_quot(a.cdiv, x) * a.cdiv.d, e >> F::kOffBits);
+    uint32_t excl[R], cnt[R], off[R], sbase[R];
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        const uint32_t tile = tile_of(r);
+        const bool tv = tile < num_tiles;
+        excl[r] = tv ? p.tile_excl[tile] : 0u;
+        cnt[r] = tv ? ld_last2(p.seg_cnt + (size_t)tile * kSegsMax + F::storage(sgl)) : 0u;
+    }
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        // Exclusive scan of the counts within each tile's group of SEGS lanes.
+        uint32_t incl = cnt[r];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= (uint32_t)d) incl += u;
+        }
+        const uint32_t first = __shfl_sync(0xFFFFFFFFu, incl - cnt[r], lbase);
+        off[r] = incl - cnt[r] - first;
+        // Where this lane's segment's entries start in its warp list.
+        sbase[r] = F::seg_base(sgl, cnt[r], lbase);
+    }
+    auto entries = [&](int r) {
+        return p.seg_ent + (size_t)tile_of(r) * kEntries + F::seg_list(sgl) * kWarpCap + sbase[r];
+    };
+    uint32_t ev[R][K];
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        const bool listed = sbase[r] + cnt[r] <= (uint32_t)kWarpCap;
+        const uint16_t* es = entries(r);
+#pragma unroll
+        for (int k = 0; k < K; k++) ev[r][k] = listed && (uint32_t)k < cnt[r] ? ld_last2(es + k) : 0u;
+    }
+
+    // Escapes of segment sgl of each round's tile, in element order.  When the
+    // chunk size is a multiple of the segment length the segment lies in one
+    // chunk, and an escape's position in it is the segment's offset in that
+    // chunk plus the entry's offset.
+    const bool seg_in_chunk = a.cdiv.d % (uint32_t)F::kSegLen == 0;
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        if (!cnt[r]) continue;
+        const uint32_t t0 = tile_of(r) * (uint32_t)kTileElems;
+        const uint32_t r0 = t0 - chunk_quot32(a.cdiv, t0) * a.cdiv.d;
+        const uint32_t g0 = excl[r] + off[r];
+        if (sbase[r] + cnt[r] <= (uint32_t)kWarpCap) {
+            const uint16_t* es = entries(r);
+            if (seg_in_chunk && (uint64_t)g0 + cnt[r] <= a.esc_capacity) {
+                const uint32_t xs = r0 + s0, base = xs - chunk_quot(a.cdiv, xs) * a.cdiv.d;
+                auto put = [&](uint32_t g, uint32_t e) {
+                    a.esc_pos[g] = (uint16_t)(base + (e & kOffMask));
+                    a.esc_val[g] = (uint8_t)(e >> F::kOffBits);
+                };
+#pragma unroll
+                for (int k = 0; k < K; k++)
+                    if ((uint32_t)k < cnt[r]) put(g0 + k, ev[r][k]);
+                for (uint32_t q = K; q < cnt[r]; q++) put(g0 + q, es[q]);
+            } else {
+                auto put = [&](uint32_t g, uint32_t e) {
+                    const uint32_t x = r0 + s0 + (e & kOffMask);
+                    put_escape(a, g, x - chunk_quot(a.cdiv, x) * a.cdiv.d, e >> F::kOffBits);
+                };
+#pragma unroll
+                for (int k = 0; k < K; k++)
+                    if ((uint32_t)k < cnt[r]) put(g0 + k, ev[r][k]);
+                for (uint32_t q = K; q < cnt[r]; q++) put(g0 + q, es[q]);
             }
         } else {
             // More escapes than the segment's entries: rebuild from the input.
+            const uint32_t len = a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
             const uint32_t end = s0 + F::kSegLen < len ? s0 + F::kSegLen : len;
             uint32_t g = g0;
             for (uint32_t l = s0; l < end; l++) {
@@ -739,49 +820,80 @@ __global__ void __launch_bounds__(kThreads, 8) place_kernel(const EncodeArgs a, 
         }
     }
 
+    // The warp's count rows and escape lists are dead once it has read them for
+    // the last time: their L2 lines (kept there by the dense pass's evict-last
+    // stores) are dropped without a write-back.  Only whole 128-byte lines
+    // inside this warp's own tiles' rows and lists are dropped.
+    auto release = [&]() {
+        __syncwarp();  // every lane's last read of the rows and lists is done
+        auto drop = [&](const uint16_t* region, uint32_t bytes_per_tile) {
+            const uint32_t t1 = min(tile0 + TPW * (uint32_t)R, num_tiles);
+            const uint64_t b0 = (uint64_t)tile0 * bytes_per_tile, b1 = (uint64_t)t1 * bytes_per_tile;
+            const char* base = reinterpret_cast<const char*>(region);
+            for (uint64_t b = b0 + 128u * lane; b + 128u <= b1; b += 32u * 128u) {
+                char* line = const_cast<char*>(base) + b;
+                if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) discard_l2_line(line);
+            }
+        };
+        drop(p.seg_cnt, 2 * kSegsMax);
+        drop(p.seg_ent, 2 * kEntries);
+    };
+
     // chunk_off at every chunk start of each of the warp's tiles: the exclusive
     // escape rank of the chunk's first element.  When the chunk size is a
     // multiple of the segment length every chunk start inside a tile is a
     // segment start (tiles and segments start at multiples of it), and the
     // lane of that segment writes it from its own offset.
-    if (a.cdiv.d % (uint32_t)F::kSegLen == 0) {
-        const uint32_t s0 = sgl * F::kSegLen, x = r0 + s0;  // x < d + kTileElems
-        const uint32_t qx = chunk_quot(a.cdiv, x);
-        if (tvalid && s0 < len && x == qx * a.cdiv.d) a.chunk_off[q0 + qx] = excl + off;
+    if (seg_in_chunk) {
+#pragma unroll
+        for (int r = 0; r < R; r++) {
+            const uint32_t tile = tile_of(r);
+            if (tile >= num_tiles) continue;
+            const uint32_t t0 = tile * (uint32_t)kTileElems;
+            const uint32_t len = a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
+            const uint32_t q0 = chunk_quot32(a.cdiv, t0), x = t0 - q0 * a.cdiv.d + s0;
+            const uint32_t qx = chunk_quot(a.cdiv, x);  // x < d + kTileElems
+            if (s0 < len && x == qx * a.cdiv.d) a.chunk_off[q0 + qx] = excl[r] + off[r];
+        }
+        release();
         return;
     }
-    for (uint32_t t = 0; t < TPW; t++) {
-        const uint32_t tl = tile0 + t;
-        if (tl >= num_tiles) break;  // warp-uniform
-        const uint32_t u0 = tl * (uint32_t)kTileElems;
-        const uint32_t ulen = a.n - u0 < (uint32_t)kTileElems ? a.n - u0 : (uint32_t)kTileElems;
-        const uint32_t uq0 = chunk_quot32(a.cdiv, u0), ur0 = u0 - uq0 * a.cdiv.d;
-        const uint32_t uexcl = __shfl_sync(0xFFFFFFFFu, excl, t * SEGS);
-        const uint16_t* uent = p.seg_ent + (size_t)tl * kEntries;
-        const uint32_t qa = ur0 ? 1u : 0u, qb = chunk_quot(a.cdiv, ur0 + ulen - 1);
-        for (uint32_t b0 = qa; b0 <= qb; b0 += 32) {
-            const uint32_t q = b0 + lane;
-            const bool valid = q <= qb;
-            const uint32_t bl = valid ? q * a.cdiv.d - ur0 : 0u;  // tile-local index of the chunk start
-            const uint32_t sg = bl / F::kSegLen;
-            const uint32_t o = __shfl_sync(0xFFFFFFFFu, off, t * SEGS + sg);
-            const uint32_t c = __shfl_sync(0xFFFFFFFFu, cnt, t * SEGS + sg);
-            const uint32_t bb = __shfl_sync(0xFFFFFFFFu, sbase, t * SEGS + sg);
-            if (valid) {
-                const uint32_t lim = bl - sg * F::kSegLen;
-                uint32_t rank = 0;
-                if (lim == 0) {
-                } else if (bb + c <= (uint32_t)kWarpCap) {
-                    const uint16_t* es = uent + F::seg_list(sg) * kWarpCap + bb;
-                    for (uint32_t r = 0; r < c; r++) rank += (es[r] & kOffMask) < lim;
-                } else {
-                    for (uint32_t l = sg * F::kSegLen; l < bl; l++)
-                        rank += !in_codebook(cbw, F::exponent_at(a, u0 + l));
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        for (uint32_t t = 0; t < TPW; t++) {
+            const uint32_t tl = tile0 + (uint32_t)r * TPW + t;
+            if (tl >= num_tiles) break;  // warp-uniform
+            const uint32_t u0 = tl * (uint32_t)kTileElems;
+            const uint32_t ulen = a.n - u0 < (uint32_t)kTileElems ? a.n - u0 : (uint32_t)kTileElems;
+            const uint32_t uq0 = chunk_quot32(a.cdiv, u0), ur0 = u0 - uq0 * a.cdiv.d;
+            const uint32_t uexcl = __shfl_sync(0xFFFFFFFFu, excl[r], t * SEGS);
+            const uint16_t* uent = p.seg_ent + (size_t)tl * kEntries;
+            const uint32_t qa = ur0 ? 1u : 0u, qb = chunk_quot(a.cdiv, ur0 + ulen - 1);
+            for (uint32_t b0 = qa; b0 <= qb; b0 += 32) {
+                const uint32_t q = b0 + lane;
+                const bool valid = q <= qb;
+                const uint32_t bl = valid ? q * a.cdiv.d - ur0 : 0u;  // tile-local chunk start
+                const uint32_t sg = bl / F::kSegLen;
+                const uint32_t o = __shfl_sync(0xFFFFFFFFu, off[r], t * SEGS + sg);
+                const uint32_t c = __shfl_sync(0xFFFFFFFFu, cnt[r], t * SEGS + sg);
+                const uint32_t bb = __shfl_sync(0xFFFFFFFFu, sbase[r], t * SEGS + sg);
+                if (valid) {
+                    const uint32_t lim = bl - sg * F::kSegLen;
+                    uint32_t rank = 0;
+                    if (lim == 0) {
+                    } else if (bb + c <= (uint32_t)kWarpCap) {
+                        const uint16_t* es = uent + F::seg_list(sg) * kWarpCap + bb;
+                        for (uint32_t q2 = 0; q2 < c; q2++) rank += (es[q2] & kOffMask) < lim;
+                    } else {
+                        for (uint32_t l = sg * F::kSegLen; l < bl; l++)
+                            rank += !in_codebook(cbw, F::exponent_at(a, u0 + l));
+                    }
+                    a.chunk_off[uq0 + q] = uexcl + o + rank;
                 }
-                a.chunk_off[uq0 + q] = uexcl + o + rank;
             }
         }
     }
+    release();
 }
 
 template <class F>
@@ -802,10 +914,10 @@ cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
     dense_kernel<F><<<(uint32_t)(tiles < wave ? tiles : wave), kThreads, smem, s>>>(a, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    prefix_kernel<<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks, F::kSegs);
+    prefix_kernel<F::kSegs><<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const uint32_t per_cta = kWarps * (32 / F::kSegs);  // tiles per placement CTA
+    const uint32_t per_cta = kWarps * (32 / F::kSegs) * F::kPlaceRounds;  // tiles per placement CTA
     place_kernel<F><<<(tiles + per_cta - 1) / per_cta, kThreads, 0, s>>>(a, p, tiles);
     return cudaGetLastError();
 }
