@@ -603,6 +603,8 @@ def main():
         "encode_gbs": round(n * elem / (enc / 1e3) / 1e9, 2),
         "decode_gbs": round(n * elem / (dec / 1e3) / 1e9, 2),
         "encode_ms": round(enc, 4), "decode_ms": round(dec, 4),
+        "encode_ms_median": round(statistics.median(res["enc_ms"]), 4),
+        "decode_ms_median": round(statistics.median(res["dec_ms"]), 4),
         "encode_hbm_frac": round(algo / (enc / 1e3) / 1e9 / peak, 4),
         "decode_hbm_frac": round(algo / (dec / 1e3) / 1e9 / peak, 4),
         "compression_ratio": round(n * elem / comp, 5), "compressed_bytes": comp,
