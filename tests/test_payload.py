@@ -134,24 +134,26 @@ def test_library_rejects_malformed_payloads():
         assert what
 
 
-def test_hand_worked_payload():
-    """A payload derived by hand from the format spec (tests/golden/
-    payload_bf16_two_slices.txt): the oracle writes exactly its bytes and
-    decodes them back, and the library's parser and size bound agree."""
+@pytest.mark.parametrize("name", ["payload_bf16_two_slices.txt", "payload_e5m2_two_slices.txt"])
+def test_hand_worked_payload(name):
+    """A payload derived by hand from the format spec (tests/golden/): the
+    oracle writes exactly its bytes and decodes them back, and the library's
+    parser and size bound agree."""
     from tests.golden_io import hex_array, int_array, load
-    fx = load("payload_bf16_two_slices.txt")
+    fx = load(name)
+    fmt = fx["format"][0]
     rows = sorted((int(k.split("@")[1]), v) for k, v in fx.items() if k.startswith("payload@"))
     assert [off for off, _ in rows] == list(range(0, 16 * len(rows), 16))
     ref = bytes(int(t, 16) for _, v in rows for t in v)
-    x = hex_array(fx["input_hex"], np.uint16)
+    x = hex_array(fx["input_hex"], np.uint16 if fmt == "bf16" else np.uint8)
     cb = [int(c) for c in fx["codebook"]]
     chunk, se = int(fx["chunk"][0]), int(fx["slice_elems"][0])
     assert len(ref) == int(fx["total_bytes"][0])
-    assert op.write(x, "bf16", chunk, se, cb) == ref
+    assert op.write(x, fmt, chunk, se, cb) == ref
     assert np.array_equal(op.decode(ref), x)
     info, slices = sz.splitzip_payload_parse(_torch_buf(ref))
     assert (info["fmt"], info["version"], info["n"], info["slice_elems"], info["chunk_size"]) == \
-        ("bf16", 1, len(x), se, chunk)
+        (fmt, 1, len(x), se, chunk)
     assert info["num_slices"] == 2 and info["n_escapes"] == int(fx["n_escapes"][0])
     assert info["total_bytes"] == len(ref)
     assert [s["n"] for s in slices] == [int(v) for v in fx["slice_n"]]
@@ -159,5 +161,5 @@ def test_hand_worked_payload():
     assert [s["off_dense"] for s in slices] == [int(v) for v in fx["slice_off_dense"]]
     assert [s["off_escapes"] for s in slices] == [int(v) for v in fx["slice_off_escapes"]]
     assert all(list(s["codebook"]) == cb for s in slices)
-    assert sz.splitzip_payload_bytes_bound(len(x), chunk, se, info["n_escapes"], "bf16") == len(ref)
+    assert sz.splitzip_payload_bytes_bound(len(x), chunk, se, info["n_escapes"], fmt) == len(ref)
     assert int_array(fx["slice_n"], np.uint64).sum() == len(x)
