@@ -118,9 +118,9 @@ uint64_t splitzip_compressed_bytes_e5m2(uint64_t n, uint32_t chunk_size, uint64_
 
 /* ---------------------------------------------------------- calibration */
 
-/* Offline calibration ("calibrated top-16 exponent codebook", arXiv abstract;
- * README sections Highlights and Codec API, where calibrate(x) returns the
- * coverage): histogram the exponents of the n elements at d_x (16-byte
+/* Offline calibration (the codebook of the 16 most frequent exponents,
+ * calibrated ahead of time: arXiv abstract; README sections Highlights and
+ * Codec API, where calibrate(x) returns the coverage): histogram the exponents of the n elements at d_x (16-byte
  * aligned bit patterns), pick the 16 most frequent (ties to the smaller
  * exponent; zero-count exponents fill up if fewer than 16 occur), and return
  * the codebook and coverage = (elements whose exponent is in the codebook) / n
