@@ -160,8 +160,14 @@ typedef struct CUevent_st *splitzip_event_t;
  * encoded and copied out while later slices are still being produced.
  * num_events: 0 (slice_ready may then be NULL; the call is exactly
  * splitzip_encode_to_host) or the number of slices, ceil(n / slice_elems).
- * The events are only waited on, never recorded or destroyed.  Other
- * arguments, errors and the payload as for splitzip_encode_to_host. */
+ * The events are only waited on, never recorded or destroyed.  Each must
+ * already be recorded when the call is made (its record enqueued on the
+ * producing stream, the work itself may still be pending): as with
+ * cudaStreamWaitEvent, the call waits for the work of the event's most recent
+ * record at that moment, and a record made later is not seen.  Like
+ * splitzip_encode_to_host the call returns once the whole payload is in host
+ * memory, so it blocks until every slice's producer work has completed.
+ * Other arguments, errors and the payload as for splitzip_encode_to_host. */
 splitzip_status splitzip_encode_to_host_events(const void* x, uint64_t n, uint32_t format,
                                                uint32_t chunk_size, const splitzip_codebook* cbs,
                                                uint32_t num_cbs, uint64_t slice_elems,

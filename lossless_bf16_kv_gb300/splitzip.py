@@ -424,8 +424,9 @@ def splitzip_encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems:
     """Encode x (GPU or pinned host tensor) slice by slice into the host uint8
     tensor `payload`.  Returns (status, payload bytes); status is OK or
     ERR_ESCAPE_OVERFLOW (payload too small: the bytes needed are returned).
-    ready_events: None, or one recorded torch.cuda.Event per slice; slice i is
-    read only after its event completes (a tensor still being produced)."""
+    ready_events: None, or one torch.cuda.Event per slice, each already
+    recorded on the producing stream; slice i is read only after the work of
+    that record completes (a tensor still being produced)."""
     fmt = _fmt_of(x, fmt)
     n = _elements(x, fmt)
     arr, k = _cbs(codebooks)
