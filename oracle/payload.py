@@ -27,6 +27,7 @@ import struct
 
 import numpy as np
 
+from . import calibrate as _calibrate
 from . import decode as _decode
 from . import encode as _encode
 
@@ -92,6 +93,17 @@ def write(x, fmt: str, chunk: int, slice_elems: int, codebooks) -> bytes:
         out += region
     assert len(out) == total
     return bytes(out)
+
+
+def write_calibrated(x, fmt: str, chunk: int, slice_elems: int) -> bytes:
+    """The payload of x with a codebook of its own for every slice: each slice
+    is calibrated on its own exponents (the top-16 of that slice, the pages'
+    calibration step applied per KV-cache layer instead of once offline) and
+    then encoded with that codebook."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    cbs = [[int(c) for c in _calibrate(x[s0:s0 + m], fmt)[0]]
+           for s0, m in _slices(x.size, slice_elems)]
+    return write(x, fmt, chunk, slice_elems, cbs)
 
 
 def read(buf: bytes):

@@ -163,3 +163,52 @@ def test_hand_worked_payload(name):
     assert all(list(s["codebook"]) == cb for s in slices)
     assert sz.splitzip_payload_bytes_bound(len(x), chunk, se, info["n_escapes"], fmt) == len(ref)
     assert int_array(fx["slice_n"], np.uint64).sum() == len(x)
+
+
+def _per_slice_input(fmt):
+    """Two slices whose exponent counts are fixed by construction, so each
+    slice's top-16 codebook (count descending, ties to the smaller exponent)
+    is known by hand.  Slice 0 (208 elements): exponent b + k appears 20 - k
+    times (k < 16) and eight other exponents once each.  Slice 1 (204
+    elements, the ragged last slice): exponents t + 2..t + 15 appear 7..20
+    times, t and t + 1 six times each (a tie), and two more exponents three
+    times in all.  Signs, mantissas and the order within a slice are random."""
+    rng = np.random.default_rng(17)
+    if fmt == "bf16":
+        b, t, rare0, rare1 = 100, 120, list(range(50, 58)), [200, 200, 5]
+    else:
+        b, t, rare0, rare1 = 0, 16, list(range(16, 24)), [0, 0, 1]
+    e0 = [b + k for k in range(16) for _ in range(20 - k)] + rare0
+    counts1 = [6, 6] + list(range(7, 21))
+    e1 = [t + k for k in range(16) for _ in range(counts1[k])] + rare1
+    cb0 = [b + k for k in range(16)]
+    cb1 = [t + k for k in range(15, 1, -1)] + [t, t + 1]
+    parts = []
+    for e in (e0, e1):
+        e = rng.permutation(np.asarray(e, np.uint32))
+        if fmt == "bf16":
+            sm = rng.integers(0, 1 << 16, e.size, dtype=np.uint32) & 0x807F
+            parts.append((sm | (e << 7)).astype(np.uint16))
+        else:
+            sm = rng.integers(0, 256, e.size, dtype=np.uint32) & 0x83
+            parts.append((sm | (e << 2)).astype(np.uint8))
+    return np.concatenate(parts), [cb0, cb1], [8, 3]
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
+def test_per_slice_calibrated_payload_codebooks(fmt):
+    """The oracle's per-slice calibrated payload: every slice carries the
+    top-16 of its own exponents (worked out by hand above), its escapes are
+    exactly the elements outside that codebook, and the rest of the payload
+    is the pinned writer's with those codebooks."""
+    x, cbs, escapes = _per_slice_input(fmt)
+    assert x.size == 412
+    buf = op.write_calibrated(x, fmt, 8, 208)
+    head, slices = op.read(buf)
+    assert [s["codebook"] for s in slices] == cbs
+    assert [s["n_escapes"] for s in slices] == escapes and head["n_escapes"] == 11
+    assert buf == op.write(x, fmt, 8, 208, cbs)
+    assert np.array_equal(op.decode(buf), x)
+    # One codebook for the whole tensor would not be either slice's.
+    whole = [int(c) for c in oracle.calibrate(x, fmt)[0]]
+    assert whole not in cbs

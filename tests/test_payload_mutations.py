@@ -5,8 +5,9 @@ Each mutation is a textual edit (of the first match) loaded as a separate
 module inside the oracle package; the real module is untouched.  A mutation
 whose target text is missing fails the test, so edits to the payload oracle
 keep this list honest.  The pins: the hand-worked payloads of tests/golden/
-(exact bytes, slice table, decode) and a round trip with one codebook per
-slice.
+(exact bytes, slice table, decode), a round trip with one codebook per
+slice, and the per-slice calibrated payloads whose codebooks are worked out by
+hand in tests/test_payload.py.
 """
 import os
 import types
@@ -34,6 +35,9 @@ MUTATIONS = {
     "header_counts_first_slice": ("chunk, sum(n_esc), total)", "chunk, n_esc[0], total)"),
     "first_codebook_for_all": ("ENTRY.pack(m, e, d, q, bytes(cb))", "ENTRY.pack(m, e, d, q, bytes(cbs[0]))"),
     "reader_chunk_off_unaligned": ("        p = _pad16(p + n_sm)\n", "        p = p + n_sm\n"),
+    "calibrated_on_whole_tensor": ("_calibrate(x[s0:s0 + m], fmt)", "_calibrate(x, fmt)"),
+    "calibrated_on_first_slice": ("_calibrate(x[s0:s0 + m], fmt)", "_calibrate(x[:m], fmt)"),
+    "calibrated_slice_cut_short": ("_calibrate(x[s0:s0 + m], fmt)", "_calibrate(x[s0:s0 + m - 16], fmt)"),
 }
 
 FIXTURES = ["payload_bf16_two_slices.txt", "payload_e5m2_two_slices.txt"]
@@ -74,7 +78,17 @@ def _pin_per_slice_codebooks(op):
     assert np.array_equal(op.decode(buf), x)
 
 
-PINS = [lambda op, n=n: _pin_fixture(op, n) for n in FIXTURES] + [_pin_per_slice_codebooks]
+def _pin_calibrated(op, fmt):
+    from tests.test_payload import _per_slice_input
+    x, cbs, escapes = _per_slice_input(fmt)
+    buf = op.write_calibrated(x, fmt, 8, 208)
+    _, slices = op.read(buf)
+    assert [s["codebook"] for s in slices] == cbs
+    assert [s["n_escapes"] for s in slices] == escapes
+
+
+PINS = ([lambda op, n=n: _pin_fixture(op, n) for n in FIXTURES] + [_pin_per_slice_codebooks]
+        + [lambda op, f=f: _pin_calibrated(op, f) for f in ("bf16", "e5m2")])
 
 
 def test_pins_hold_for_the_real_payload_oracle():
