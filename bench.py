@@ -13,6 +13,10 @@ needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
+At N=1 the line also carries the other seeded workloads (configs 1, 2, 4
+and its 5-20% escape variant, and the FP8 E5M2 prefill KV), each timed the
+same way with fewer steps, under "configs".
+
 Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are independent
 replicas: each rank encodes/decodes its own copy, with no collective on the
 data path (weak scaling); a barrier brackets the timed region and the time is
@@ -293,16 +297,119 @@ def run_gpu(args):
         "algo_bytes": algorithmic_bytes(fmt, n, chunk, E), "elem": elem,
     }
     if args.e2e:
-        del streams, y
+        del streams, y, ws
         torch.cuda.empty_cache()
         res["e2e"] = run_e2e(x, cb, fmt, chunk, K, dev, world)
         if rank == 0 and world == 1:
             res["transfer"] = run_transfer(x, cb, fmt, chunk, dev)
-    if rank == 0 and world == 1 and args.cpu_baseline:
-        res["cpu_sample"] = synth.raw_bits(x[: min(n, args.cpu_sample_elems)]).cpu()
+    if rank == 0 and world == 1 and args.configs:
+        del x
+        torch.cuda.empty_cache()
+        res["configs"] = run_configs(args.workload, max(3, min(K, 50)), dev)
     if world > 1:
         dist.destroy_process_group()
     return res
+
+
+# The other seeded workloads, each timed like the headline one and reported
+# beside it: config 1 (N(0,1)), config 2 (one KV layer), config 4 and its
+# 5-20% escape variant, config 5 (FP8 E5M2 prefill KV).
+CONFIG_WORKLOADS = ("n01_1024x4096", "kv_layer_32k", "kv_prefill_64L_16k",
+                    "escape_stress_t15", "escape_stress_t15_u4", "kv_prefill_64L_16k_e5m2")
+L2_BYTES = 129e6
+
+
+def time_codec(x, cal, w, steps, dev, flush=None):
+    """Calibrate on cal, then time `steps` encode + decode pairs of x with CUDA
+    events on the launching stream (L2 flushed between steps when the tensor
+    would otherwise stay in it).  Checks the round trip and returns the
+    per-step times and stream figures."""
+    import torch
+
+    from lossless_bf16_kv_gb300 import splitzip as sz
+    from lossless_bf16_kv_gb300 import synth
+
+    fmt, chunk = w.fmt, w.chunk
+    n = x.numel()
+    ws = sz.alloc_workspace(max(n, cal.numel()), dev)
+    cb, coverage = sz.splitzip_calibrate(cal, ws, fmt)
+    streams = sz.alloc_streams(n, chunk, fmt, n // 32 + 1024, dev)
+    sz.splitzip_encode(x, chunk, cb, streams, ws, fmt)
+    status, E = sz.splitzip_encode_status(ws)
+    if status == sz.ERR_ESCAPE_OVERFLOW:
+        streams = sz.alloc_streams(n, chunk, fmt, E, dev)
+        sz.splitzip_encode(x, chunk, cb, streams, ws, fmt)
+        status, E = sz.splitzip_encode_status(ws)
+    if status != sz.OK:
+        _fail(f"{w.name}: encode status {status}")
+    y = torch.empty_like(x)
+    for _ in range(3):
+        sz.splitzip_encode(x, chunk, cb, streams, ws, fmt)
+        sz.splitzip_decode(streams, n, chunk, cb, y, fmt, n_escapes=E)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        sz.splitzip_encode(x, chunk, cb, streams, ws, fmt)
+        ev[i][1].record()
+        if flush is not None:   # decode would read streams the encode just left in L2
+            flush.fill_((i + 1) & 0xFF)
+        ev[i][2].record()
+        sz.splitzip_decode(streams, n, chunk, cb, y, fmt, n_escapes=E)
+        ev[i][3].record()
+    torch.cuda.synchronize()
+    st_after, E_after = sz.splitzip_encode_status(ws)
+    if st_after != sz.OK or E_after != E or not torch.equal(synth.raw_bits(x), synth.raw_bits(y)):
+        _fail(f"{w.name}: timed round trip failed (status {st_after}, E {E_after} vs {E})")
+    enc = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
+    dec = [ev[i][2].elapsed_time(ev[i][3]) for i in range(steps)]
+    return enc, dec, E, cb, coverage
+
+
+def config_figures(w, n, E, enc, dec, peak) -> dict:
+    from lossless_bf16_kv_gb300 import splitzip as sz
+    elem = 2 if w.fmt == "bf16" else 1
+    algo = algorithmic_bytes(w.fmt, n, w.chunk, E)
+    e, d = statistics.mean(enc), statistics.mean(dec)
+    comp = sz.splitzip_compressed_bytes(n, w.chunk, E, w.fmt)
+    return {"workload": w.name, "format": w.fmt, "shape": list(w.shape), "elements": n,
+            "steps": len(enc), "encode_ms": round(e, 4), "decode_ms": round(d, 4),
+            "encode_ms_median": round(statistics.median(enc), 4),
+            "decode_ms_median": round(statistics.median(dec), 4),
+            "encode_gbs": round(n * elem / (e / 1e3) / 1e9, 2),
+            "decode_gbs": round(n * elem / (d / 1e3) / 1e9, 2),
+            "encode_hbm_frac": round(algo / (e / 1e3) / 1e9 / peak, 4),
+            "decode_hbm_frac": round(algo / (d / 1e3) / 1e9 / peak, 4),
+            "algorithmic_bytes": algo, "n_escapes": E, "escape_rate": round(E / n, 6),
+            "compression_ratio": round(n * elem / comp, 5),
+            "l2": ("input larger than L2: no flush" if n * elem > L2_BYTES else
+                   "L2 flushed (256 MB write) before each encode and each decode; small "
+                   "tensors are bound by launch latency, not HBM")}
+
+
+def run_configs(skip: str, steps: int, dev) -> list:
+    """Every other seeded workload, timed and checked like the headline one."""
+    import torch
+
+    from lossless_bf16_kv_gb300 import synth
+    peak, _ = measured_peak_hbm()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = []
+    for name in CONFIG_WORKLOADS:
+        if name == skip:
+            continue
+        w = synth.WORKLOADS[name]
+        x = w.make(dev).reshape(-1)
+        cal = w.make_calib(dev).reshape(-1)
+        n = x.numel()
+        big = n * (2 if w.fmt == "bf16" else 1) > L2_BYTES
+        enc, dec, E, _, _ = time_codec(x, cal, w, steps, dev, None if big else flush)
+        out.append(config_figures(w, n, E, enc, dec, peak))
+        del x, cal
+        torch.cuda.empty_cache()
+    return out
 
 
 def transfer_slice_elems(n: int, chunk: int) -> int:
@@ -333,7 +440,7 @@ def run_e2e(x, cb, fmt, chunk, K, dev, world):
     scratch = sz.alloc_transfer_scratch(se, chunk, fmt, dev)
     streams = [torch.cuda.Stream(dev) for _ in range(3)]
     payload, nbytes = sz.encode_to_host(hx, chunk, cb, se, scratch, streams, fmt)
-    steps = max(1, min(K, 10))
+    steps = K
 
     def step():
         st, nb = sz.splitzip_encode_to_host(hx, chunk, cb, se, payload, scratch, streams, fmt)
@@ -464,81 +571,88 @@ def host_threads() -> int:
         return max(1, os.cpu_count() or 1)
 
 
-def cpu_baseline(sample_bits_torch, fmt, chunk, cb, target_s: float):
-    """The oracle as it stands on a bounded sample of the workload, sized to
-    take about target_s of single-thread CPU time: once on one thread, and once
-    on every host core as concurrent runs over chunk-aligned shards (the
-    chunk-range sharding of the format; the oracle's code is the same)."""
+# Both CPU measurements -- the GPU line's cpu_baseline and the reference arm --
+# time the oracle on one sample: the first CPU_SAMPLE_ELEMS elements of the
+# workload, drawn on the host by the workload's own generator (for the prefill
+# KV workloads, its first layers), with the codebook the oracle calibrates on
+# the workload's calibration recipe drawn the same way.
+CPU_SAMPLE_ELEMS = 1 << 28
+
+
+def cpu_sample(w):
+    """(bits, codebook, description) of the oracle's bounded sample of w."""
     import numpy as np
-    bits = sample_bits_torch.numpy().reshape(-1)
-    bits = bits.view(np.uint16) if fmt == "bf16" else bits.view(np.uint8)
-    probe = bits[: min(bits.size, 1 << 22)]
-    per_elem = time_oracle(probe, fmt, chunk, cb) / probe.size
-    m = int(min(bits.size, max(1 << 22, target_s / per_elem)))
-    m -= m % chunk if m > chunk else 0
-    sec = time_oracle(bits[:m], fmt, chunk, cb)
+    import torch
+
+    import oracle
+    from lossless_bf16_kv_gb300 import synth
+    if w.name.startswith("kv_prefill"):
+        dt = torch.bfloat16 if w.fmt == "bf16" else torch.float8_e5m2
+        layers = max(1, min(w.shape[0], CPU_SAMPLE_ELEMS // math.prod(w.shape[1:])))
+        x = synth.kv_cache(layers, w.shape[2], seed=0, device="cpu", dtype=dt)
+        cal = synth.kv_cache(w.shape[0], 1024, seed=1, device="cpu", dtype=dt)
+        what = f"first {layers} of {w.shape[0]} layers"
+    else:
+        x, cal = w.make("cpu"), w.make_calib("cpu")
+        what = "the whole tensor"
+    bits = synth.raw_bits(x).numpy().reshape(-1)[:CPU_SAMPLE_ELEMS]
+    cbits = synth.raw_bits(cal).numpy().reshape(-1)
+    if w.fmt == "bf16":
+        bits, cbits = bits.view(np.uint16), cbits.view(np.uint16)
+    cb, _ = oracle.calibrate(cbits, w.fmt)
+    desc = (f"{bits.size} elements ({what}) of the workload drawn on the host by the same "
+            f"generator; one oracle encode+decode round trip per run")
+    return np.ascontiguousarray(bits), cb, desc
+
+
+def cpu_baseline(w, target_cpu_s: float):
+    """The oracle as it stands on the shared sample: on every host core as
+    concurrent runs over chunk-aligned shards (the chunk-range sharding of the
+    format; the oracle's code is the same), repeated until about target_cpu_s
+    of CPU time has been spent, and once on one thread."""
+    bits, cb, desc = cpu_sample(w)
     T = host_threads()
-    sec_t = time_oracle_sharded(bits[:m], fmt, chunk, cb, T)
-    elem = 2 if fmt == "bf16" else 1
-    return {"value": round(m * elem / sec_t / 1e9, 4), "unit": "GB/s", "cores": T,
+    runs, wall = 0, 0.0
+    while runs == 0 or wall * T < target_cpu_s:
+        wall += time_oracle_sharded(bits, w.fmt, w.chunk, cb, T)
+        runs += 1
+    sec1 = time_oracle(bits, w.fmt, w.chunk, cb)
+    elem = 2 if w.fmt == "bf16" else 1
+    return {"value": round(bits.size * elem * runs / wall / 1e9, 4), "unit": "GB/s", "cores": T,
             "kind": "oracle",
-            "sample": f"first {m} elements of the workload, one encode+decode round trip, "
-                      f"{T} concurrent oracle runs over chunk-aligned shards ({sec_t:.2f} s wall)",
-            "single_thread": {"value": round(m * elem / sec / 1e9, 4), "cores": 1,
-                              "seconds": round(sec, 2)}}
+            "sample": f"{desc}; {T} concurrent oracle runs over chunk-aligned shards, mean of "
+                      f"{runs} runs ({wall:.2f} s wall)",
+            "single_thread": {"value": round(bits.size * elem / sec1 / 1e9, 4), "cores": 1,
+                              "seconds": round(sec1, 2)}}
 
 
 # ----------------------------------------------------------- reference arm
 
 def run_reference(args):
     """The oracle (plain C) on the host cores: each step is one encode + decode
-    round trip of a bounded sample of the same workload, as concurrent oracle
-    runs over chunk-aligned shards, one per host core."""
-    import numpy as np
-
-    import oracle
+    round trip of the shared bounded sample of the workload, as concurrent
+    oracle runs over chunk-aligned shards, one per host core."""
     from lossless_bf16_kv_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
-    fmt, chunk = w.fmt, w.chunk
-    dt = None
-    if w.name.startswith("kv_prefill"):
-        import torch
-        dt = torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2
-        x = synth.kv_cache(1, 16384, seed=0, device="cpu", dtype=dt)   # first layer's shape
-        cal = synth.kv_cache(1, 1024, seed=1, device="cpu", dtype=dt)
-    else:
-        x, cal = w.make("cpu"), w.make_calib("cpu")
-    bits = synth.raw_bits(x).numpy().reshape(-1)
-    bits = bits.view(np.uint16) if fmt == "bf16" else bits
-    cbits = synth.raw_bits(cal).numpy().reshape(-1)
-    cbits = cbits.view(np.uint16) if fmt == "bf16" else cbits
-    cb, _ = oracle.calibrate(cbits, fmt)
-    probe = bits[: 1 << 20]
-    per_elem = time_oracle(probe, fmt, chunk, cb) / probe.size
+    bits, cb, desc = cpu_sample(w)
     T = host_threads()
-    budget = 120.0 / max(1, args.steps + args.warmup)          # whole run within ~2 minutes
-    m = int(min(bits.size, max(1 << 20, budget * T / per_elem)))
-    m -= m % chunk if m > chunk else 0
-    sample = np.ascontiguousarray(bits[:m])
     for _ in range(args.warmup):
-        time_oracle_sharded(sample, fmt, chunk, cb, T)
+        time_oracle_sharded(bits, w.fmt, w.chunk, cb, T)
     secs = 0.0
     for _ in range(args.steps):
-        secs += time_oracle_sharded(sample, fmt, chunk, cb, T)
-    elem = 2 if fmt == "bf16" else 1
-    value = m * elem * args.steps / secs / 1e9
-    desc = (f"first {m} elements of a CPU-drawn sample of the workload (same generator); "
-            f"one oracle encode+decode round trip per step, {T} concurrent oracle runs over "
-            f"chunk-aligned shards")
+        secs += time_oracle_sharded(bits, w.fmt, w.chunk, cb, T)
+    elem = 2 if w.fmt == "bf16" else 1
+    value = bits.size * elem * args.steps / secs / 1e9
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": w.fmt, "data": "synthetic",
         "config": workload_config(w, args.gpus),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": T, "kind": "oracle",
-                         "sample": desc},
+                         "sample": f"{desc}; {T} concurrent oracle runs over chunk-aligned "
+                                   f"shards per step"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -566,8 +680,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--cpu-sample-elems", type=int, default=1 << 30)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0,
+                    help="CPU time (threads x wall) the cpu_baseline spends at least")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip timing the other seeded workloads")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, _ = dist_env()
@@ -598,7 +714,7 @@ def main():
         "metric": METRIC, "value": round(res["value_gbs"], 2), "unit": "GB/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(res["total_s"] * 1e3 / K, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": res["fmt"], "data": "synthetic",
         "config": workload_config(w, world),
         "encode_gbs": round(n * elem / (enc / 1e3) / 1e9, 2),
         "decode_gbs": round(n * elem / (dec / 1e3) / 1e9, 2),
@@ -629,9 +745,10 @@ def main():
         line["e2e"] = res["e2e"]
     if "transfer" in res:
         line["transfer"] = res["transfer"]
-    if "cpu_sample" in res:
-        line["cpu_baseline"] = cpu_baseline(res["cpu_sample"], res["fmt"], res["chunk"],
-                                            res["codebook"], args.cpu_seconds)
+    if "configs" in res:
+        line["configs"] = res["configs"]
+    if world == 1 and args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
 

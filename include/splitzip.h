@@ -171,10 +171,33 @@ splitzip_status splitzip_encode_e5m2(const void *d_x, uint64_t n, uint32_t chunk
                                      const splitzip_codebook *cb, const splitzip_streams *out,
                                      void *d_workspace, splitzip_stream_t s);
 
+/* splitzip_encode with the codebook in DEVICE memory: d_codebook points to
+ * the 16 codebook bytes (4-byte aligned), for example as written by
+ * splitzip_calibrate_async on the same stream.  The pages calibrate the
+ * codebook ahead of time and keep it as codec state (README sections
+ * Highlights and Codec API; arXiv abstract); reading it on the device lets a
+ * caller calibrate per tensor or per KV-cache layer and encode right after,
+ * with no host round trip.  The bytes are read when the kernels run (the
+ * codebook may still be being written by earlier work on s).  Since the host
+ * cannot check them, the encode checks them itself: a codebook whose 16
+ * entries are not distinct (or, for E5M2, not all below 32) makes
+ * splitzip_encode_status report SPLITZIP_ERR_INVALID_ARG, the streams then
+ * being invalid (every write still stays inside the given buffers).  Other
+ * arguments, results and errors as for splitzip_encode[_e5m2]. */
+splitzip_status splitzip_encode_devcb(const void *d_x, uint64_t n, uint32_t chunk_size,
+                                      const uint8_t *d_codebook, const splitzip_streams *out,
+                                      void *d_workspace, splitzip_stream_t s);
+splitzip_status splitzip_encode_devcb_e5m2(const void *d_x, uint64_t n, uint32_t chunk_size,
+                                           const uint8_t *d_codebook,
+                                           const splitzip_streams *out, void *d_workspace,
+                                           splitzip_stream_t s);
+
 /* Synchronise s and report the most recent finished encode on d_workspace:
- * SPLITZIP_OK, SPLITZIP_ERR_ESCAPE_OVERFLOW, SPLITZIP_ERR_TIMEOUT or
- * SPLITZIP_ERR_WORKSPACE (the later codes win; the last two mean the streams
- * are invalid).  *n_escapes_out (may be NULL) receives E, the escapes needed. */
+ * SPLITZIP_OK, SPLITZIP_ERR_ESCAPE_OVERFLOW, SPLITZIP_ERR_INVALID_ARG (a
+ * device codebook given to splitzip_encode_devcb[_e5m2] was not valid),
+ * SPLITZIP_ERR_TIMEOUT or SPLITZIP_ERR_WORKSPACE (the later codes win; all but
+ * the first two mean the streams are invalid).  *n_escapes_out (may be NULL)
+ * receives E, the escapes needed. */
 splitzip_status splitzip_encode_status(const void *d_workspace, splitzip_stream_t s,
                                        uint64_t *n_escapes_out);
 
@@ -192,6 +215,17 @@ splitzip_status splitzip_decode(const splitzip_streams *in, uint64_t n, uint32_t
 splitzip_status splitzip_decode_e5m2(const splitzip_streams *in, uint64_t n,
                                      uint32_t chunk_size, const splitzip_codebook *cb,
                                      void *d_y, splitzip_stream_t s);
+
+/* splitzip_decode with the codebook in DEVICE memory (16 bytes, 4-byte
+ * aligned), read when the kernel runs -- the decode side of
+ * splitzip_encode_devcb.  The bytes are not checked: with a codebook other
+ * than the one the streams were encoded with the values are unspecified, but
+ * every access stays inside the given buffers. */
+splitzip_status splitzip_decode_devcb(const splitzip_streams *in, uint64_t n, uint32_t chunk_size,
+                                      const uint8_t *d_codebook, void *d_y, splitzip_stream_t s);
+splitzip_status splitzip_decode_devcb_e5m2(const splitzip_streams *in, uint64_t n,
+                                           uint32_t chunk_size, const uint8_t *d_codebook,
+                                           void *d_y, splitzip_stream_t s);
 
 /* ------------------------------------------------ encode without workspace */
 

@@ -126,7 +126,14 @@ size_t splitzip_transfer_scratch_bytes(uint32_t format, uint64_t slice_elems,
  *    call finds out which with cudaPointerGetAttributes and, for host input,
  *    copies each slice to the device first.
  * cbs: num_cbs codebooks in host memory: 1 (shared by all slices) or one per
- *    slice (for example a codebook calibrated per KV-cache layer).
+ *    slice (for example a codebook calibrated per KV-cache layer); or cbs NULL
+ *    and num_cbs 0: every slice is calibrated on the device, right before it
+ *    is encoded, on its own elements (splitzip_calibrate_async, then
+ *    splitzip_encode_devcb), and the slice table carries the codebook each
+ *    slice got.  This is the pages' calibration step (a top-16 codebook fixed
+ *    ahead of the encode: README sections Highlights and Codec API) taken per
+ *    layer, so that a codebook follows the KV statistics of its own layer
+ *    with no host round trip.
  * slice_elems: a multiple of chunk_size and of 16 (so every slice starts on a
  *    chunk and on a 16-byte boundary), at least chunk_size.
  * d_scratch: splitzip_transfer_scratch_bytes(format, slice_elems, chunk_size)

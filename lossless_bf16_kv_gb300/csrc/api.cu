@@ -59,18 +59,21 @@ inline splitzip_status from_cuda(cudaError_t e) {
     return e == cudaSuccess ? SPLITZIP_OK : SPLITZIP_ERR_CUDA;
 }
 
+// Exactly one of cb (host memory, checked here) and dcb (device memory, 4-byte
+// aligned, checked by the encode itself) gives the codebook.
 splitzip_status encode_impl(const void* d_x, uint64_t n, uint32_t chunk,
-                            const splitzip_codebook* cb, const splitzip_streams* out,
-                            void* ws, cudaStream_t s, bool e5m2, uint32_t spin_limit,
-                            uint32_t flags) {
-    if (!d_x || !cb || !out || !ws) return SPLITZIP_ERR_INVALID_ARG;
+                            const splitzip_codebook* cb, const uint8_t* dcb,
+                            const splitzip_streams* out, void* ws, cudaStream_t s, bool e5m2,
+                            uint32_t spin_limit, uint32_t flags) {
+    if (!d_x || (!cb == !dcb) || !out || !ws) return SPLITZIP_ERR_INVALID_ARG;
+    if (dcb && (!aligned(dcb, 4) || (flags & kTestPipelined))) return SPLITZIP_ERR_INVALID_ARG;
     if (!count_ok(n) || !chunk_ok(chunk)) return SPLITZIP_ERR_INVALID_ARG;
     if (!out->codes || !out->signman || !out->chunk_off) return SPLITZIP_ERR_INVALID_ARG;
     if (out->esc_capacity && (!out->esc_pos || !out->esc_val)) return SPLITZIP_ERR_INVALID_ARG;
     if (!aligned(d_x, 16) || !aligned(out->codes, 16) || !aligned(out->signman, 16) ||
         !aligned(out->chunk_off, 4) || !aligned(out->esc_pos, 2) || !aligned(ws, 16))
         return SPLITZIP_ERR_INVALID_ARG;
-    if (!codebook_ok(cb, e5m2)) return SPLITZIP_ERR_INVALID_ARG;
+    if (cb && !codebook_ok(cb, e5m2)) return SPLITZIP_ERR_INVALID_ARG;
     EncodeArgs a;
     a.x = static_cast<const uint8_t*>(d_x);
     a.n = (uint32_t)n;
@@ -86,21 +89,27 @@ splitzip_status encode_impl(const void* d_x, uint64_t n, uint32_t chunk,
     a.num_tiles = (uint32_t)ceil_div(n, (uint64_t)encode_tile_elems(e5m2));
     a.spin_limit = spin_limit ? spin_limit : kDefaultSpinLimit;
     a.test_flags = flags;
-    pack_codebook(cb, a.cbw);
+    if (cb) pack_codebook(cb, a.cbw);
+    else a.cbw[0] = a.cbw[1] = a.cbw[2] = a.cbw[3] = 0;
+    a.dcb = dcb;
     return from_cuda((flags & kTestPipelined) ? launch_encode(a, e5m2, s)
                                               : launch_encode_multi(a, e5m2, s));
 }
 
+// Exactly one of cb (host memory, checked here) and dcb (device memory,
+// 4-byte aligned, not checked) gives the codebook.
 splitzip_status decode_impl(const splitzip_streams* in, uint64_t n, uint32_t chunk,
-                            const splitzip_codebook* cb, void* d_y, cudaStream_t s, bool e5m2) {
-    if (!in || !cb || !d_y) return SPLITZIP_ERR_INVALID_ARG;
+                            const splitzip_codebook* cb, const uint8_t* dcb, void* d_y,
+                            cudaStream_t s, bool e5m2) {
+    if (!in || (!cb == !dcb) || !d_y) return SPLITZIP_ERR_INVALID_ARG;
+    if (dcb && !aligned(dcb, 4)) return SPLITZIP_ERR_INVALID_ARG;
     if (!count_ok(n) || !chunk_ok(chunk)) return SPLITZIP_ERR_INVALID_ARG;
     if (!in->codes || !in->signman || !in->chunk_off) return SPLITZIP_ERR_INVALID_ARG;
     if (in->esc_capacity && (!in->esc_pos || !in->esc_val)) return SPLITZIP_ERR_INVALID_ARG;
     if (!aligned(d_y, 16) || !aligned(in->codes, 16) || !aligned(in->signman, 16) ||
         !aligned(in->chunk_off, 4) || !aligned(in->esc_pos, 2))
         return SPLITZIP_ERR_INVALID_ARG;
-    if (!codebook_ok(cb, e5m2)) return SPLITZIP_ERR_INVALID_ARG;
+    if (cb && !codebook_ok(cb, e5m2)) return SPLITZIP_ERR_INVALID_ARG;
     DecodeArgs a;
     a.codes = in->codes;
     a.signman = in->signman;
@@ -113,7 +122,9 @@ splitzip_status decode_impl(const splitzip_streams* in, uint64_t n, uint32_t chu
     a.nchunks = (uint32_t)ceil_div(n, chunk);
     a.y = static_cast<uint8_t*>(d_y);
     a.num_tiles = (uint32_t)ceil_div(n, (uint64_t)decode_tile_elems(e5m2));
-    pack_codebook(cb, a.cbw);
+    if (cb) pack_codebook(cb, a.cbw);
+    else a.cbw[0] = a.cbw[1] = a.cbw[2] = a.cbw[3] = 0;
+    a.dcb = dcb;
     return from_cuda(launch_decode(a, e5m2, s));
 }
 
@@ -248,14 +259,16 @@ splitzip_status splitzip_encode(const void* d_x, uint64_t n, uint32_t chunk_size
                                 const splitzip_codebook* cb, const splitzip_streams* out,
                                 void* d_workspace, splitzip_stream_t s) {
     TraceRange trace("splitzip_encode");
-    return encode_impl(d_x, n, chunk_size, cb, out, d_workspace, (cudaStream_t)s, false, 0, 0);
+    return encode_impl(d_x, n, chunk_size, cb, nullptr, out, d_workspace, (cudaStream_t)s, false,
+                       0, 0);
 }
 
 splitzip_status splitzip_encode_e5m2(const void* d_x, uint64_t n, uint32_t chunk_size,
                                      const splitzip_codebook* cb, const splitzip_streams* out,
                                      void* d_workspace, splitzip_stream_t s) {
     TraceRange trace("splitzip_encode_e5m2");
-    return encode_impl(d_x, n, chunk_size, cb, out, d_workspace, (cudaStream_t)s, true, 0, 0);
+    return encode_impl(d_x, n, chunk_size, cb, nullptr, out, d_workspace, (cudaStream_t)s, true,
+                       0, 0);
 }
 
 splitzip_status splitzip_encode_test(const void* d_x, uint64_t n, uint32_t chunk_size,
@@ -265,8 +278,8 @@ splitzip_status splitzip_encode_test(const void* d_x, uint64_t n, uint32_t chunk
     const uint32_t limit = opts ? opts->spin_limit : 0;
     const uint32_t flags =
         opts ? (opts->flags & (SPLITZIP_TEST_STALL_FIRST_TILE | SPLITZIP_TEST_PIPELINED)) : 0;
-    return encode_impl(d_x, n, chunk_size, cb, out, d_workspace, (cudaStream_t)s, is_e5m2 != 0,
-                       limit, flags);
+    return encode_impl(d_x, n, chunk_size, cb, nullptr, out, d_workspace, (cudaStream_t)s,
+                       is_e5m2 != 0, limit, flags);
 }
 
 splitzip_status splitzip_encode_status(const void* d_workspace, splitzip_stream_t s,
@@ -288,6 +301,7 @@ splitzip_status splitzip_encode_status(const void* d_workspace, splitzip_stream_
     if (n_escapes_out) *n_escapes_out = host.last_escapes;
     if (host.last_status & kStatusBadWorkspace) return SPLITZIP_ERR_WORKSPACE;
     if (host.last_status & kStatusTimeout) return SPLITZIP_ERR_TIMEOUT;
+    if (host.last_status & kStatusBadCodebook) return SPLITZIP_ERR_INVALID_ARG;
     if (host.last_status & kStatusOverflow) return SPLITZIP_ERR_ESCAPE_OVERFLOW;
     return SPLITZIP_OK;
 }
@@ -295,16 +309,45 @@ splitzip_status splitzip_encode_status(const void* d_workspace, splitzip_stream_
 splitzip_status splitzip_decode(const splitzip_streams* in, uint64_t n, uint32_t chunk_size,
                                 const splitzip_codebook* cb, void* d_y, splitzip_stream_t s) {
     TraceRange trace("splitzip_decode");
-    return decode_impl(in, n, chunk_size, cb, d_y, (cudaStream_t)s, false);
+    return decode_impl(in, n, chunk_size, cb, nullptr, d_y, (cudaStream_t)s, false);
 }
 
 splitzip_status splitzip_decode_e5m2(const splitzip_streams* in, uint64_t n,
                                      uint32_t chunk_size, const splitzip_codebook* cb, void* d_y,
                                      splitzip_stream_t s) {
     TraceRange trace("splitzip_decode_e5m2");
-    return decode_impl(in, n, chunk_size, cb, d_y, (cudaStream_t)s, true);
+    return decode_impl(in, n, chunk_size, cb, nullptr, d_y, (cudaStream_t)s, true);
 }
 
-int splitzip_version(void) { return 100; }
+splitzip_status splitzip_encode_devcb(const void* d_x, uint64_t n, uint32_t chunk_size,
+                                      const uint8_t* d_codebook, const splitzip_streams* out,
+                                      void* d_workspace, splitzip_stream_t s) {
+    TraceRange trace("splitzip_encode_devcb");
+    return encode_impl(d_x, n, chunk_size, nullptr, d_codebook, out, d_workspace,
+                       (cudaStream_t)s, false, 0, 0);
+}
+
+splitzip_status splitzip_encode_devcb_e5m2(const void* d_x, uint64_t n, uint32_t chunk_size,
+                                           const uint8_t* d_codebook, const splitzip_streams* out,
+                                           void* d_workspace, splitzip_stream_t s) {
+    TraceRange trace("splitzip_encode_devcb_e5m2");
+    return encode_impl(d_x, n, chunk_size, nullptr, d_codebook, out, d_workspace,
+                       (cudaStream_t)s, true, 0, 0);
+}
+
+splitzip_status splitzip_decode_devcb(const splitzip_streams* in, uint64_t n, uint32_t chunk_size,
+                                      const uint8_t* d_codebook, void* d_y, splitzip_stream_t s) {
+    TraceRange trace("splitzip_decode_devcb");
+    return decode_impl(in, n, chunk_size, nullptr, d_codebook, d_y, (cudaStream_t)s, false);
+}
+
+splitzip_status splitzip_decode_devcb_e5m2(const splitzip_streams* in, uint64_t n,
+                                           uint32_t chunk_size, const uint8_t* d_codebook,
+                                           void* d_y, splitzip_stream_t s) {
+    TraceRange trace("splitzip_decode_devcb_e5m2");
+    return decode_impl(in, n, chunk_size, nullptr, d_codebook, d_y, (cudaStream_t)s, true);
+}
+
+int splitzip_version(void) { return 110; }
 
 }  // extern "C"

@@ -108,6 +108,38 @@ __device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
     asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v));
 }
 
+// ------------------------------------------------------------- codebook
+//
+// The 16 codebook bytes as four little-endian words: from the launch
+// parameters, or from device memory (4-byte aligned) when dcb is not null --
+// a codebook that an earlier kernel on the stream (device-side calibration)
+// wrote, read without a round trip through the host.
+__device__ __forceinline__ void codebook_words(const uint8_t* dcb, const uint32_t (&param)[4],
+                                               uint32_t (&w)[4]) {
+    if (dcb) {
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(dcb);
+#pragma unroll
+        for (int q = 0; q < 4; q++) w[q] = __ldg(p + q);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; q++) w[q] = param[q];
+    }
+}
+
+// Whether the codebook words hold 16 distinct exponents, each at most
+// max_exp (255 for BF16, 31 for E5M2).
+__device__ __forceinline__ bool codebook_valid(const uint32_t (&w)[4], uint32_t max_exp) {
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < 16; k++) {
+        const uint32_t e = (w[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+        ok = ok && e <= max_exp;
+#pragma unroll
+        for (int j = 0; j < k; j++) ok = ok && ((w[j >> 2] >> (8 * (j & 3))) & 0xFFu) != e;
+    }
+    return ok;
+}
+
 // ------------------------------------------------------------- division
 //
 // q = floor(x / d) as (x * m) >> 33 with m = ceil(2^33 / d), exact for

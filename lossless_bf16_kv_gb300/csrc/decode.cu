@@ -568,10 +568,12 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) decode_kernel(const D
     __shared__ uint16_t pairs[256];
     Luts lut;
     lut.pairs = pairs;
-    if constexpr (F::kPairs) build_pairs<F>(pairs, a.cbw);
+    uint32_t cbw[4];
+    codebook_words(a.dcb, a.cbw, cbw);
+    if constexpr (F::kPairs) build_pairs<F>(pairs, cbw);
 #pragma unroll
     for (int q = 0; q < 4; q++) {  // F::exp_byte of each byte of the codebook words
-        const uint32_t w = a.cbw[q];
+        const uint32_t w = cbw[q];
         lut.cb[q] = F::exp_byte(w & 0xFFu) | (F::exp_byte((w >> 8) & 0xFFu) << 8) |
                     (F::exp_byte((w >> 16) & 0xFFu) << 16) | (F::exp_byte(w >> 24) << 24);
     }

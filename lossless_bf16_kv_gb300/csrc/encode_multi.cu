@@ -89,6 +89,11 @@ __device__ __forceinline__ void warp_scan_excl(uint32_t p, uint32_t& excl, uint3
     p31 = __shfl_sync(0xFFFFFFFFu, p, 31);
 }
 
+// Codebook entry 0 (the exponent of code 0), from wherever the codebook is.
+__device__ __forceinline__ uint32_t codebook_entry0(const EncodeArgs& a) {
+    return a.dcb ? (uint32_t)__ldg(a.dcb) : (a.cbw[0] & 0xFFu);
+}
+
 // ------------------------------------------------------------------- BF16
 //
 // Thread t's groups of 8 at tile offsets k*2048 + 8t (k < 4): each warp load
@@ -203,7 +208,7 @@ struct Bf16Dense {
     // The last, partial tile (element by element at its end).
     static __device__ __forceinline__ void process_partial(const EncodeArgs& a, const Tables& tb,
                                                            uint32_t t0, Keep& kp) {
-        const uint32_t pad = (a.cbw[0] & 0xFFu) << 7;  // exponent cb[0], sign 0, mantissa 0: code 0
+        const uint32_t pad = codebook_entry0(a) << 7;  // exponent cb[0], sign 0, mantissa 0: code 0
         const uint16_t* xs = reinterpret_cast<const uint16_t*>(a.x);
         kp.cnt = 0;
 #pragma unroll
@@ -422,7 +427,7 @@ struct E5m2Dense {
             w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
             w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
         } else {
-            const uint32_t pad = (a.cbw[0] & 0x1Fu) << 2;  // exponent cb[0], sign 0, mantissa 0
+            const uint32_t pad = (codebook_entry0(a) & 0x1Fu) << 2;  // exponent cb[0], sign 0, mantissa 0
             const uint32_t rem = a.n - i;
 #pragma unroll
             for (int m = 0; m < 8; m++) {
@@ -546,7 +551,11 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
     constexpr int L = F::kLoads, S = kDenseStages;
     extern __shared__ uint4 ring[];  // [S][L][kThreads]
     __shared__ typename F::Tables tables;
-    F::build_tables(tables, a.cbw);
+    {
+        uint32_t cbw[4];
+        codebook_words(a.dcb, a.cbw, cbw);
+        F::build_tables(tables, cbw);
+    }
     // With F::kKeepLists, counts and list entries stay in L2 for the prefix and
     // placement passes while the tensor streams through.
     const uint64_t keep = F::kKeepLists ? l2_evict_last_policy() : 0u;
@@ -613,7 +622,7 @@ __device__ void prefix_finished(const EncodeArgs& a, uint32_t epoch) {
     }
 }
 
-template <int SEGS>
+template <int SEGS, uint32_t kMaxExp>
 __global__ void __launch_bounds__(kThreads) prefix_kernel(const EncodeArgs a, const MultiPtrs p,
                                                           uint32_t num_tiles, uint32_t num_blocks) {
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
@@ -688,6 +697,11 @@ __global__ void __launch_bounds__(kThreads) prefix_kernel(const EncodeArgs a, co
         a.chunk_off[a.nchunks] = total;
         hdr->last_escapes = total;
         if ((uint64_t)total > a.esc_capacity) atomicOr(&hdr->status, kStatusOverflow);
+        if (a.dcb) {  // a codebook from device memory is checked here, once per encode
+            uint32_t cbw[4];
+            codebook_words(a.dcb, a.cbw, cbw);
+            if (!codebook_valid(cbw, kMaxExp)) atomicOr(&hdr->status, kStatusBadCodebook);
+        }
     }
     __syncthreads();
     if (tid == 0) prefix_finished(a, epoch);
@@ -729,7 +743,6 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
     constexpr uint32_t kOffMask = (1u << F::kOffBits) - 1u;
     constexpr uint32_t SEGS = F::kSegs, TPW = 32 / F::kSegs;
     constexpr int R = F::kPlaceRounds, K = F::kPreload;
-    const uint32_t cbw[4] = {a.cbw[0], a.cbw[1], a.cbw[2], a.cbw[3]};
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW * R;
     if (tile0 >= num_tiles) return;  // warp-uniform
@@ -807,6 +820,8 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
             }
         } else {
             // More escapes than the segment's entries: rebuild from the input.
+            uint32_t cbw[4];
+            codebook_words(a.dcb, a.cbw, cbw);
             const uint32_t len = a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
             const uint32_t end = s0 + F::kSegLen < len ? s0 + F::kSegLen : len;
             uint32_t g = g0;
@@ -885,6 +900,8 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
                         const uint16_t* es = uent + F::seg_list(sg) * kWarpCap + bb;
                         for (uint32_t q2 = 0; q2 < c; q2++) rank += (es[q2] & kOffMask) < lim;
                     } else {
+                        uint32_t cbw[4];
+                        codebook_words(a.dcb, a.cbw, cbw);
                         for (uint32_t l = sg * F::kSegLen; l < bl; l++)
                             rank += !in_codebook(cbw, F::exponent_at(a, u0 + l));
                     }
@@ -914,7 +931,7 @@ cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
     dense_kernel<F><<<(uint32_t)(tiles < wave ? tiles : wave), kThreads, smem, s>>>(a, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    prefix_kernel<F::kSegs><<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks);
+    prefix_kernel<F::kSegs, F::kExpMask><<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const uint32_t per_cta = kWarps * (32 / F::kSegs) * F::kPlaceRounds;  // tiles per placement CTA

@@ -12,6 +12,7 @@ namespace splitzip {
 constexpr uint32_t kTestStallFirstTile = 1u;    // tile 0 never publishes (test hook)
 constexpr uint32_t kTestPipelined = 2u;         // test hook: run the single-launch pipeline
 constexpr uint32_t kStatusBadWorkspace = 4u;    // a CTA drew a ticket past the grid
+constexpr uint32_t kStatusBadCodebook = 8u;     // a device-resident codebook was not valid
 constexpr uint32_t kDefaultSpinLimit = 1u << 21;  // look-back polls (load + 32 ns sleep): ~1 s
 
 struct EncodeArgs {
@@ -30,6 +31,7 @@ struct EncodeArgs {
     uint32_t spin_limit;
     uint32_t test_flags;
     uint32_t cbw[4];     // codebook bytes, 4 per word, little-endian
+    const uint8_t* dcb = nullptr;  // or, when not null, the 16 codebook bytes in device memory
 };
 
 struct DecodeArgs {
@@ -45,6 +47,7 @@ struct DecodeArgs {
     uint8_t* y;          // output bit patterns, 16-byte aligned
     uint32_t num_tiles;
     uint32_t cbw[4];
+    const uint8_t* dcb = nullptr;  // when not null: the codebook in device memory instead of cbw
 };
 
 struct CalibArgs {

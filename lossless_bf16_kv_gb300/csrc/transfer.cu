@@ -294,13 +294,16 @@ splitzip_status splitzip_encode_to_host_events(const void* x, uint64_t n, uint32
                                                const splitzip_event_t* slice_ready,
                                                uint32_t num_events) {
     splitzip::TraceRange trace("splitzip_encode_to_host");
-    if (!x || !cbs || !h_payload || !payload_bytes || !d_scratch) return SPLITZIP_ERR_INVALID_ARG;
+    if (!x || !h_payload || !payload_bytes || !d_scratch) return SPLITZIP_ERR_INVALID_ARG;
+    // No codebooks: every slice is calibrated on the device right before its encode.
+    const bool calibrate_slices = cbs == nullptr && num_cbs == 0;
+    if (!cbs && !calibrate_slices) return SPLITZIP_ERR_INVALID_ARG;
     if (!format_ok(format) || !chunk_ok(chunk_size) || n == 0 || n > SPLITZIP_MAX_ELEMENTS)
         return SPLITZIP_ERR_INVALID_ARG;
     if (slice_elems < chunk_size || slice_elems % chunk_size || slice_elems % 16)
         return SPLITZIP_ERR_INVALID_ARG;
     const uint32_t S = (uint32_t)ceil_div(n, slice_elems);
-    if (num_cbs != 1 && num_cbs != S) return SPLITZIP_ERR_INVALID_ARG;
+    if (!calibrate_slices && num_cbs != 1 && num_cbs != S) return SPLITZIP_ERR_INVALID_ARG;
     if (num_events != 0 && (num_events != S || !slice_ready)) return SPLITZIP_ERR_INVALID_ARG;
     for (uint32_t i = 0; i < num_cbs; i++)
         if (!codebook_ok(cbs[i], format)) return SPLITZIP_ERR_INVALID_ARG;
@@ -334,7 +337,8 @@ splitzip_status splitzip_encode_to_host_events(const void* x, uint64_t n, uint32
 
     std::vector<splitzip_slice_entry> table(S);
     // Slice i's device status word is copied into the first bytes of its own
-    // slice-table entry (host memory the caller pinned; rewritten at the end).
+    // slice-table entry (host memory the caller pinned; rewritten at the end),
+    // and a codebook calibrated on the device into the entry's codebook field.
     auto status_slot = [&](uint32_t i) {
         return out + SPLITZIP_PAYLOAD_HEADER_BYTES + (uint64_t)i * SPLITZIP_PAYLOAD_SLICE_ENTRY_BYTES;
     };
@@ -369,13 +373,15 @@ splitzip_status splitzip_encode_to_host_events(const void* x, uint64_t n, uint32
         std::memcpy(&stj, status_slot(j), 4);
         if (stj & 2u) return SPLITZIP_ERR_TIMEOUT;
         if (stj & 4u) return SPLITZIP_ERR_WORKSPACE;
+        if (stj & 8u) return SPLITZIP_ERR_CUDA;  // cannot happen: calibration yields a valid codebook
         const uint64_t ej = ej32;
         if (ej > nj) return SPLITZIP_ERR_CUDA;  // cannot happen for a finished encode
         table[j].n = nj;
         table[j].n_escapes = ej;
         table[j].off_dense = dense_off;
         table[j].off_escapes = esc_off;
-        table[j].cb = cbs[num_cbs == 1 ? 0 : j];
+        if (calibrate_slices) std::memcpy(table[j].cb.exp, status_slot(j) + 32, 16);
+        else table[j].cb = cbs[num_cbs == 1 ? 0 : j];
         const uint64_t region = align16(3 * ej);
         if (!overflow && esc_off + region <= payload_capacity) {
             if (ej) {
@@ -421,17 +427,31 @@ splitzip_status splitzip_encode_to_host_events(const void* x, uint64_t n, uint32
         ss.esc_pos = reinterpret_cast<uint16_t*>(B.esc);
         ss.esc_val = B.esc + 2 * slice_elems;
         ss.esc_capacity = ni;
-        const splitzip_codebook& cb = cbs[num_cbs == 1 ? 0 : i];
-        st = format == SPLITZIP_FORMAT_BF16
-                 ? splitzip_encode(src, ni, chunk_size, &cb, &ss, B.ws, s_compute)
-                 : splitzip_encode_e5m2(src, ni, chunk_size, &cb, &ss, B.ws, s_compute);
+        splitzip::WsHeader* hdr = reinterpret_cast<splitzip::WsHeader*>(B.ws);
+        if (calibrate_slices) {
+            // The slice's own top-16, left in its workspace header for the encode.
+            st = format == SPLITZIP_FORMAT_BF16
+                     ? splitzip_calibrate_async(src, ni, hdr->cal_cb, &hdr->cal_covered, B.ws, s_compute)
+                     : splitzip_calibrate_async_e5m2(src, ni, hdr->cal_cb, &hdr->cal_covered, B.ws,
+                                                     s_compute);
+            if (st != SPLITZIP_OK) break;
+            st = format == SPLITZIP_FORMAT_BF16
+                     ? splitzip_encode_devcb(src, ni, chunk_size, hdr->cal_cb, &ss, B.ws, s_compute)
+                     : splitzip_encode_devcb_e5m2(src, ni, chunk_size, hdr->cal_cb, &ss, B.ws, s_compute);
+        } else {
+            const splitzip_codebook& cb = cbs[num_cbs == 1 ? 0 : i];
+            st = format == SPLITZIP_FORMAT_BF16
+                     ? splitzip_encode(src, ni, chunk_size, &cb, &ss, B.ws, s_compute)
+                     : splitzip_encode_e5m2(src, ni, chunk_size, &cb, &ss, B.ws, s_compute);
+        }
         if (st != SPLITZIP_OK) break;
         uint8_t* dst = out + slice_dense_offset(PL, format, slice_elems, chunk_size, i);
-        const splitzip::WsHeader* hdr = reinterpret_cast<const splitzip::WsHeader*>(B.ws);
         e = cudaEventRecord(enc_done[b], sc);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, enc_done[b], 0);
         if (e == cudaSuccess) e = cudaMemcpyAsync(dst, B.dense, DL.bytes, cudaMemcpyDeviceToHost, sd);
         if (e == cudaSuccess) e = cudaMemcpyAsync(status_slot(i), &hdr->last_status, 4, cudaMemcpyDeviceToHost, sd);
+        if (e == cudaSuccess && calibrate_slices)
+            e = cudaMemcpyAsync(status_slot(i) + 32, hdr->cal_cb, 16, cudaMemcpyDeviceToHost, sd);
         if (e == cudaSuccess) e = cudaEventRecord(dense_done[b], sd);
         if (e != cudaSuccess) { st = SPLITZIP_ERR_CUDA; break; }
         if (i >= 1) st = place_escapes(i - 1);

@@ -105,6 +105,10 @@ def library() -> ctypes.CDLL:
         "splitzip_encode_status": (st, [vp, vp, ctypes.POINTER(u64)]),
         "splitzip_decode": (st, [sp, u64, u32, cbp, vp, vp]),
         "splitzip_decode_e5m2": (st, [sp, u64, u32, cbp, vp, vp]),
+        "splitzip_encode_devcb": (st, [vp, u64, u32, vp, sp, vp, vp]),
+        "splitzip_encode_devcb_e5m2": (st, [vp, u64, u32, vp, sp, vp, vp]),
+        "splitzip_decode_devcb": (st, [sp, u64, u32, vp, vp, vp]),
+        "splitzip_decode_devcb_e5m2": (st, [sp, u64, u32, vp, vp, vp]),
         "splitzip_encode_noalloc": (st, [vp, u64, u32, cbp, sp, vp, vp]),
         "splitzip_version": (i32, []),
         "splitzip_payload_bytes_bound": (u64, [u32, u64, u32, u64, u64]),
@@ -341,6 +345,45 @@ def splitzip_decode(streams: dict, n: int, chunk: int, codebook, y: torch.Tensor
               _stream(stream)), "splitzip_decode")
 
 
+def _devcb(cb: torch.Tensor) -> ctypes.c_void_p:
+    """A device codebook: 16 uint8 on the GPU, 4-byte aligned (as
+    splitzip_calibrate_async writes it)."""
+    if cb.dtype != torch.uint8 or cb.numel() < 16:
+        raise SplitZipError(ERR_INVALID_ARG, "a device codebook is 16 uint8 values")
+    return _dev(cb, "codebook")
+
+
+def splitzip_encode_devcb(x: torch.Tensor, chunk: int, cb_dev: torch.Tensor, streams: dict,
+                          workspace: torch.Tensor, fmt: str | None = None, stream=None):
+    """splitzip_encode with the codebook read from device memory (cb_dev, e.g.
+    the output of splitzip_calibrate_async); asynchronous.  An invalid device
+    codebook is reported by splitzip_encode_status as ERR_INVALID_ARG."""
+    fmt = _fmt_of(x, fmt)
+    n = _elements(x, fmt)
+    fn = library().splitzip_encode_devcb if fmt == "bf16" else library().splitzip_encode_devcb_e5m2
+    if n and chunk > 0:
+        _need_streams(streams, n, chunk, fmt)
+        _need(workspace, splitzip_workspace_bytes(n, chunk), "workspace")
+    s = _streams(streams)
+    _check(fn(_dev(x, "x"), n, chunk, _devcb(cb_dev), ctypes.byref(s),
+              _dev(workspace, "workspace"), _stream(stream)), "splitzip_encode_devcb")
+
+
+def splitzip_decode_devcb(streams: dict, n: int, chunk: int, cb_dev: torch.Tensor,
+                          y: torch.Tensor, fmt: str = "bf16", stream=None,
+                          n_escapes: int | None = None):
+    """splitzip_decode with the codebook read from device memory; asynchronous."""
+    if n > 0 and chunk > 0:
+        _need_streams(streams, n, chunk, fmt)
+        _need(y, n * _ELEM[fmt], "y")
+    s = _streams(streams)
+    if n_escapes is not None:
+        s.esc_capacity = min(s.esc_capacity, n_escapes)
+    fn = library().splitzip_decode_devcb if fmt == "bf16" else library().splitzip_decode_devcb_e5m2
+    _check(fn(ctypes.byref(s), n, chunk, _devcb(cb_dev), _dev(y, "y"), _stream(stream)),
+           "splitzip_decode_devcb")
+
+
 def splitzip_version() -> int:
     return int(library().splitzip_version())
 
@@ -389,7 +432,10 @@ def alloc_transfer_scratch(slice_elems: int, chunk: int, fmt: str = "bf16",
 
 
 def _cbs(codebooks) -> tuple:
-    """A shared codebook (16 ints) or one codebook per slice."""
+    """A shared codebook (16 ints), one codebook per slice, or None (every
+    slice calibrated on the device)."""
+    if codebooks is None:
+        return None, 0
     seq = codebooks.tolist() if hasattr(codebooks, "tolist") else list(codebooks)
     if len(seq) == 16 and all(isinstance(v, int) for v in seq):
         seq = [seq]
@@ -424,6 +470,8 @@ def splitzip_encode_to_host(x: torch.Tensor, chunk: int, codebooks, slice_elems:
     """Encode x (GPU or pinned host tensor) slice by slice into the host uint8
     tensor `payload`.  Returns (status, payload bytes); status is OK or
     ERR_ESCAPE_OVERFLOW (payload too small: the bytes needed are returned).
+    codebooks: one shared codebook, one per slice, or None to calibrate every
+    slice on the device just before it is encoded.
     ready_events: None, or one torch.cuda.Event per slice, each already
     recorded on the producing stream; slice i is read only after the work of
     that record completes (a tensor still being produced)."""
