@@ -6,26 +6,23 @@
 // reassemble sign, exponent and mantissa, and put the raw exponent of every
 // escape back at its position; the result is bitwise identical to the input.
 //
-// One launch, no communication between CTAs; the only CTA barrier follows the
-// BF16 table build at the start.  Warps walk contiguous segments (1024 BF16
-// or 2048 E5M2 elements) grid-stride:
+// One launch, no communication between CTAs.  Warps walk contiguous segments
+// (1024 BF16 or 2048 E5M2 elements) grid-stride:
 //   - the dense streams (codes, sign+mantissa) of the next segment are loaded
-//     into registers (BF16), or reach shared memory through a per-warp ring of
-//     kDecodeStages slots filled by cp.async (E5M2: 16 bytes per lane per
-//     copy, fully coalesced, kDecodeStages - 1 segments ahead);
-//   - the segment's slice [lo, hi) of the escape stream is found two segments
-//     ahead (chunk_off at a chunk start, else a warp-wide search of the
+//     into registers (BF16), or reach shared memory through a per-warp ring
+//     filled by cp.async (E5M2: 16 bytes per lane per copy, coalesced);
+//   - the segment's slice [lo, hi) of the escape stream is found ahead of the
+//     segment (chunk_off at a chunk start, else a warp-wide search of the
 //     ascending positions inside the chunk) and its first 32 escapes are
 //     loaded one segment ahead;
-//   - each lane decodes its exponents in registers: BF16 two codes at a time
-//     from a 256-entry shared-memory table of code bytes (built per CTA from
-//     the codebook), E5M2 a code word (eight codes) at a time by byte permutes
-//     of the 16 entries held in four registers;
-//   - a segment with escapes parks its exponent words in shared memory, each
-//     lane holding an escape overwrites that element's exponent byte, and the
-//     words are read back (escapes beyond the first 32 of a segment are read
-//     in further batches);
-//   - SWAR reassembly and 16-byte stores.
+//   - BF16: each lane decodes its exponents two codes at a time from a
+//     256-entry shared-memory table of code bytes (built per CTA from the
+//     codebook); a segment with escapes parks its exponent words in shared
+//     memory, each lane holding an escape overwrites that element's exponent
+//     byte, and the words are read back; SWAR reassembly and 16-byte stores;
+//   - E5M2: a code word (eight codes) at a time by byte permutes of the 16
+//     entries held in four registers, fields spread by shifts and selects,
+//     16-byte stores; each escape is then written over its output byte.
 // All escape metadata is clamped, so malformed streams cannot make the kernel
 // read or write out of bounds.
 #include <cstdint>
@@ -37,21 +34,22 @@ namespace splitzip {
 namespace {
 
 // Exponents of the eight codes of a code word (code k in nibble k of cw)
-// from the codebook held in four words (cb0 = entries 0..3, ..., cb3 =
-// entries 12..15): codes 0..3 into lo, codes 4..7 into hi.  Entries 0..7 and
-// 8..15 are each one byte permute; a third permute in sign-replicate mode
-// turns bit 3 of each code into a 0x00/0xFF byte mask that picks between the
-// two.  The masks are formed once for all eight codes (a permute reads only
-// the low 16 bits of its selector).
-__device__ __forceinline__ void cb_lookup8(const uint32_t (&cb)[4], uint32_t cw, uint32_t& lo,
-                                           uint32_t& hi) {
-    const uint32_t sel = cw & 0x77777777u;
-    const uint32_t t = cw & 0x88888888u;
-    const uint32_t u = t | (t >> 3);  // nibble 9 where bit 3 is set, else 0
-    const uint32_t sh = sel >> 16, uh = u >> 16;
-    const uint32_t m0 = prmt(0x00008000u, 0u, u), m1 = prmt(0x00008000u, 0u, uh);
-    lo = (prmt(cb[2], cb[3], sel) & m0) | (prmt(cb[0], cb[1], sel) & ~m0);
-    hi = (prmt(cb[2], cb[3], sh) & m1) | (prmt(cb[0], cb[1], sh) & ~m1);
+// from the codebook held in four words (cb[0] = entries 0..3, ..., cb[3] =
+// entries 12..15), every entry already shifted into the E5M2 exponent field
+// (bits 2..6, so bit 7 of each entry is 0).  One byte permute reads entries
+// 0..7 with the codes as selectors: a code of 8 or more has selector bit 3
+// set, which makes the permute replicate bit 7 of the chosen entry -- 0.  A
+// second permute reads entries 8..15 with selector bit 3 flipped, so codes
+// below 8 give 0 there.  The exponent bytes of codes 0..3 are lo_a | lo_b,
+// of codes 4..7 hi_a | hi_b (a permute reads the low 16 bits of its
+// selector).
+__device__ __forceinline__ void cb_lookup8(const uint32_t (&cb)[4], uint32_t cw, uint32_t& lo_a,
+                                           uint32_t& lo_b, uint32_t& hi_a, uint32_t& hi_b) {
+    const uint32_t cx = cw ^ 0x88888888u;
+    lo_a = prmt(cb[0], cb[1], cw);
+    lo_b = prmt(cb[2], cb[3], cx);
+    hi_a = prmt(cb[0], cb[1], cw >> 16);
+    hi_b = prmt(cb[2], cb[3], cx >> 16);
 }
 
 // Exponents of all 256 code bytes, two per entry (code byte c holds one
@@ -71,13 +69,10 @@ __device__ __forceinline__ void build_pairs(uint16_t* t, const uint32_t (&cbw)[4
     __syncthreads();
 }
 
-// The codebook as each format's decode reads it: BF16 through the pair table
-// in shared memory, E5M2 from four registers holding F::exp_byte of each entry
-// (its segments already stream through shared memory, and more shared-memory
-// loads measured slower there).
+// The codebook as the BF16 decode reads it: through the pair table in shared
+// memory.
 struct Luts {
     const uint16_t* pairs;
-    uint32_t cb[4];
 };
 
 // Four exponent bytes of the four codes in c16 (two code bytes).
@@ -211,117 +206,23 @@ __device__ __forceinline__ void patch_escapes(const DecodeArgs& a, const EscBatc
     __syncwarp();  // the next segment's patch area writes come after these reads
 }
 
-constexpr int kDecodeStages = 2;
-
-// Shared memory of a decode CTA: the patch area ([warp][exponent word][lane])
-// and, for a format decoded through the ring, the ring ([stage][warp][stage
-// bytes]) in front of it.
+// Shared memory of a BF16 decode CTA: the patch area ([warp][exponent
+// word][lane]).
 template <class F>
 constexpr size_t decode_smem_bytes() {
-    return (F::kRing ? (size_t)kDecodeStages * kWarps * F::kStageBytes : 0) +
-           (size_t)kWarps * F::kExWords * 32 * 4;
+    return (size_t)kWarps * F::kExWords * 32 * 4;
 }
 
-// Segment loop shared by both formats.  F provides:
-//   kSeg, kStageBytes, kExWords   elements per segment, dense bytes per
-//                                 segment (codes first, then sign+mantissa),
-//                                 exponent words per lane
-//   sm_offset(s0)                 byte offset of the segment's sign+mantissa
+// Segment loop of the BF16 decode.  F provides:
+//   kSeg, kExWords                elements per segment, exponent words per lane
 //   struct Dense / struct Ex      the lane's dense words / exponent words e[]
-//   read(stage, lane)             -> Dense, from a staged full segment
 //   load(a, s0, lane)             -> Dense, straight from global memory
-//   decode(cb, d, ex)             exponents of the lane's elements
+//   decode(lut, d, ex)            exponents of the lane's elements
 //   locate(local, q, l, byte)     exponent word q of lane l, byte, of element
 //                                 `local` of the segment
 //   store(a, s0, s1, lane, d, ex)
-template <class F>
-__device__ __forceinline__ void decode_segments(const DecodeArgs& a, uint8_t* smem,
-                                                const Luts& lut) {
-    constexpr int S = kDecodeStages;
-    constexpr uint32_t kPieces = F::kStageBytes / 16;
-    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t warps = gridDim.x * kWarps;
-    const uint32_t nseg = (uint32_t)(((uint64_t)a.n + F::kSeg - 1) / F::kSeg);  // n may be 2^32 - 1
-    const uint32_t full_segs = a.n / (uint32_t)F::kSeg;
-    uint8_t* ring = smem + (size_t)warp * F::kStageBytes;  // stage s at ring + s * kWarps * kStageBytes
-    uint32_t* pex = reinterpret_cast<uint32_t*>(smem + (size_t)S * kWarps * F::kStageBytes) +
-                    (size_t)warp * F::kExWords * 32;
-    uint32_t seg = blockIdx.x * kWarps + warp;
-    if (seg >= nseg) return;  // warp-uniform
-    const uint64_t pol = l2_evict_first_policy();  // the streams are read once
-
-    // Lanes copy the segment's dense bytes 16 at a time; a lane may read bytes
-    // another lane copied, so every read of a stage follows this lane's wait
-    // and a __syncwarp, and every refill follows a __syncwarp after the reads.
-    auto fill = [&](uint32_t sg, int stage) {
-        if (sg < full_segs) {
-            const uint32_t s0 = sg * (uint32_t)F::kSeg;
-            uint8_t* dst = ring + (size_t)stage * kWarps * F::kStageBytes;
-#pragma unroll
-            for (uint32_t q = 0; q < (kPieces + 31) / 32; q++) {
-                const uint32_t piece = q * 32 + lane;
-                if (piece < kPieces) {
-                    const uint32_t off = piece * 16;
-                    const uint8_t* src = off < (uint32_t)F::kCodeBytes
-                                             ? a.codes + s0 / 2 + off
-                                             : a.signman + F::sm_offset(s0) + (off - F::kCodeBytes);
-                    cp_async16_hint(dst + off, src, pol);
-                }
-            }
-        }
-        cp_async_commit();  // one group per segment, empty when not staged
-    };
-    auto bounds = [&](uint32_t sg, uint32_t& lo, uint32_t& hi) {
-        lo = hi = 0;
-        if (sg >= nseg) return;  // warp-uniform
-        const uint32_t s0 = sg * (uint32_t)F::kSeg;
-        const uint32_t s1 = a.n - s0 < (uint32_t)F::kSeg ? a.n : s0 + F::kSeg;
-        lo = escape_bound(a, s0);
-        hi = max(lo, escape_bound(a, s1));
-    };
-
-#pragma unroll
-    for (int st = 0; st < S; st++) fill(seg + st * warps, st);
-    uint32_t lo, hi, lo1, hi1;
-    bounds(seg, lo, hi);
-    bounds(seg + warps, lo1, hi1);
-    EscBatch eb = load_batch(a, lo, hi);
-    int stage = 0;
-    while (true) {
-        const uint32_t s0 = seg * (uint32_t)F::kSeg;
-        const uint32_t s1 = a.n - s0 < (uint32_t)F::kSeg ? a.n : s0 + F::kSeg;
-        const uint32_t next = seg + warps;
-        const bool more = next < nseg;
-        uint32_t lo2, hi2;
-        bounds(next + warps, lo2, hi2);  // two segments ahead
-        typename F::Dense d;
-        if (seg < full_segs) {
-            cp_async_wait<S - 1>();  // this segment's group (the oldest pending) has landed
-            __syncwarp();
-            d = F::read(ring + (size_t)stage * kWarps * F::kStageBytes, lane);
-        } else {
-            d = F::load(a, s0, lane);
-        }
-        typename F::Ex ex;
-        F::decode(lut, d, ex);
-        if (lo < hi) patch_escapes<F>(a, eb, lo, hi, s0, s1, pex, ex);  // warp-uniform
-        if (more) eb = load_batch(a, lo1, hi1);
-        F::store(a, s0, s1, lane, d, ex);
-        __syncwarp();  // every lane has read the stage before it is refilled
-        fill(seg + S * warps, stage);
-        stage = stage + 1 == S ? 0 : stage + 1;
-        if (!more) break;
-        seg = next;
-        lo = lo1;
-        hi = hi1;
-        lo1 = lo2;
-        hi1 = hi2;
-    }
-    cp_async_wait<0>();
-}
-
-// The same segment loop with the next segment's dense words prefetched into
-// registers instead of a shared-memory ring (one segment ahead).
+// The next segment's dense words are prefetched into registers (one segment
+// ahead), its escape slice found and its first 32 escapes loaded one ahead.
 template <class F>
 __device__ __forceinline__ void decode_segments_regs(const DecodeArgs& a, uint8_t* smem,
                                                      const Luts& lut) {
@@ -415,7 +316,6 @@ struct Bf16Seg {
         }
         return d;
     }
-    static constexpr bool kPairs = true;  // exponents from the pair table
     static constexpr int kMinBlocks = 4;  // resident CTAs per SM: 64 registers
     static __device__ __forceinline__ uint32_t exp_byte(uint32_t e) { return e; }
     static __device__ __forceinline__ void decode(const Luts& lut, const Dense& d, Ex& ex) {
@@ -453,114 +353,289 @@ struct Bf16Seg {
 
 // ------------------------------------------------------------------- E5M2
 //
-// Segment [s0, s0 + 2048); lane l holds the groups of 32 at s0 + 1024 k + 32 l
-// (k < 2): 16 code bytes and 12 bytes of packed 3-bit fields in, 32 output
-// bytes out per group.  Stage layout: the segment's 1024 code bytes, then its
-// 768 bytes of 3-bit fields.
-struct E5m2Seg {
-    // Dense words through the two-stage ring: at 2^31 elements this measured
-    // 0.94 ms against 0.96 ms with register prefetch.
-    static constexpr bool kRing = true;
-    static constexpr int kSeg = 2048;
-    static constexpr int kGroups = 2;
-    static constexpr int kCodeBytes = kSeg / 2;
-    static constexpr int kStageBytes = kCodeBytes + kSeg * 3 / 8;
-    static constexpr int kExWords = 8 * kGroups;
-    struct Dense {
-        uint4 code[kGroups];
-        uint32_t smw[kGroups][3];
-    };
-    struct Ex {
-        uint32_t e[kExWords];  // word 8k + m: elements 4m..4m+3 of group k
-    };
-    static __device__ __forceinline__ uint32_t sm_offset(uint32_t s0) { return s0 / 8 * 3; }
-    static __device__ __forceinline__ Dense read(const uint8_t* stage, uint32_t lane) {
-        Dense d;
-#pragma unroll
-        for (int k = 0; k < kGroups; k++) {
-            d.code[k] = *reinterpret_cast<const uint4*>(stage + 512 * k + 16 * lane);
-            const uint32_t* w =
-                reinterpret_cast<const uint32_t*>(stage + kCodeBytes + 384 * k + 12 * lane);
-            d.smw[k][0] = w[0];
-            d.smw[k][1] = w[1];
-            d.smw[k][2] = w[2];
-        }
-        return d;
+// Segment [s0, s0 + 2048) per warp; lane l holds the groups of 32 elements at
+// s0 + 1024 k + 32 l (k < 2): 16 code bytes and 12 bytes of packed 3-bit
+// fields in, 32 output bytes out per group.  The dense bytes of a segment
+// (its 1024 code bytes, then its 768 field bytes) reach shared memory through
+// a per-warp ring of kE5Stages slots filled by cp.async, 16 bytes per lane
+// per copy (coalesced, evict-first in L2), kE5Stages - 1 segments ahead.
+// Each output word is assembled in registers and stored; the escapes of the
+// segment are then written over their elements as single bytes (sign and
+// mantissa from the staged fields, the raw exponent from the escape stream),
+// ordered after the word stores by a __syncwarp.
+namespace e5 {
+
+constexpr int kSeg = 2048;
+constexpr int kCodeBytes = kSeg / 2;
+constexpr int kFieldBytes = kSeg * 3 / 8;
+constexpr int kStageBytes = kCodeBytes + kFieldBytes;  // 1792
+constexpr int kPieces = kStageBytes / 16;              // 112 copies of 16 bytes
+constexpr int kStages = 2;
+constexpr int kMinBlocks = 6;  // resident CTAs per SM
+
+// a where m is set, b elsewhere (one LOP3).
+__device__ __forceinline__ uint32_t sel(uint32_t a, uint32_t b, uint32_t m) {
+    return (a & m) | (b & ~m);
+}
+
+// One output word (four E5M2 values).  lo: the word's four 3-bit fields at
+// bits 0..11 of lo, and the same fields at bits 10..21 of hi (other bits of
+// lo and hi are ignored); ea | eb: the four exponents in place.  The fields
+// are spread to the bottom of each byte in two select steps (f0, f1 stay,
+// f2, f3 move up 10; then f1, f3 move up 5), the sign bits move to bit 7.
+__device__ __forceinline__ uint32_t word(uint32_t lo, uint32_t hi, uint32_t ea, uint32_t eb) {
+    const uint32_t t = sel(hi, lo, 0xFFFF0000u);       // f0 f1 at 0..5, f2 f3 at 16..21
+    const uint32_t f = sel(t << 5, t, 0x07000700u);    // field j at bits 8j..8j+2
+    const uint32_t u = sel(f << 5, f, 0x80808080u);    // sign bit of byte j at 8j+7
+    return ((u & 0x83838383u) | ea) | eb;
+}
+
+// The eight output words of a group: codes c (16 bytes), fields w0..w2
+// (12 bytes, field j at bits 3j..3j+2 of the 96-bit little-endian stream).
+__device__ __forceinline__ void group(const uint32_t (&cb)[4], const uint4& c, uint32_t w0,
+                                      uint32_t w1, uint32_t w2, uint32_t (&out)[8]) {
+    uint32_t a[8], b[8];
+    cb_lookup8(cb, c.x, a[0], b[0], a[1], b[1]);
+    cb_lookup8(cb, c.y, a[2], b[2], a[3], b[3]);
+    cb_lookup8(cb, c.z, a[4], b[4], a[5], b[5]);
+    cb_lookup8(cb, c.w, a[6], b[6], a[7], b[7]);
+    // Word m's fields start at stream bit 12 m.
+    out[0] = word(w0, w0 << 10, a[0], b[0]);
+    out[1] = word(w0 >> 12, w0 >> 2, a[1], b[1]);
+    out[2] = word(__funnelshift_r(w0, w1, 24), __funnelshift_r(w0, w1, 14), a[2], b[2]);
+    out[3] = word(w1 >> 4, w1 << 6, a[3], b[3]);
+    out[4] = word(w1 >> 16, w1 >> 6, a[4], b[4]);
+    out[5] = word(__funnelshift_r(w1, w2, 28), __funnelshift_r(w1, w2, 18), a[5], b[5]);
+    out[6] = word(w2 >> 8, w2 << 2, a[6], b[6]);
+    out[7] = word(w2 >> 20, w2 >> 10, a[7], b[7]);
+}
+
+// The 3-bit field of element j of a field stream f of `bytes` bytes.
+__device__ __forceinline__ uint32_t field_at(const uint8_t* f, uint64_t j) {
+    const uint64_t bit = 3 * j;
+    const uint32_t sh = (uint32_t)(bit & 7);
+    uint32_t v = f[bit >> 3];
+    if (sh > 5) v |= (uint32_t)f[(bit >> 3) + 1] << 8;  // the field runs into the next byte
+    return (v >> sh) & 7u;
+}
+
+// Escape slice [lo, hi) of a segment.  When both ends of the segment are
+// chunk starts the two chunk_off loads are returned unclamped, to be clamped
+// (finish) an iteration later, when their values have arrived; otherwise the
+// slice is searched (and clamped) at once.
+struct Slice {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ Slice slice_issue(const DecodeArgs& a, uint32_t sg, uint32_t nseg) {
+    Slice b{0u, 0u};
+    if (sg >= nseg) return b;  // warp-uniform
+    const uint32_t s0 = sg * (uint32_t)kSeg;
+    const uint32_t s1 = a.n - s0 < (uint32_t)kSeg ? a.n : s0 + kSeg;
+    const uint32_t c0 = chunk_quot32(a.cdiv, s0);
+    const uint32_t c1 = s1 >= a.n ? a.nchunks : chunk_quot32(a.cdiv, s1);
+    if (s0 == c0 * a.cdiv.d && (s1 >= a.n || s1 == c1 * a.cdiv.d)) {
+        b.lo = a.chunk_off[c0];
+        b.hi = a.chunk_off[c1];
+    } else {
+        b.lo = escape_bound(a, s0);
+        b.hi = max(b.lo, escape_bound(a, s1));
     }
-    static __device__ __forceinline__ Dense load(const DecodeArgs& a, uint32_t s0, uint32_t lane) {
-        Dense d;
-        const uint32_t s1 = a.n - s0 < (uint32_t)kSeg ? a.n : s0 + kSeg;
-        const bool full = s1 - s0 == (uint32_t)kSeg;
+    return b;
+}
+__device__ __forceinline__ Slice slice_finish(const DecodeArgs& a, Slice b) {
+    const uint32_t lo = (uint64_t)b.lo < a.esc_count ? b.lo : (uint32_t)a.esc_count;
+    const uint32_t hi = (uint64_t)b.hi < a.esc_count ? b.hi : (uint32_t)a.esc_count;
+    return Slice{lo, max(lo, hi)};
+}
+
+// Up to 32 escapes of a segment, one per lane, as loaded one segment ahead:
+// pv = position in chunk | raw exponent << 16 (0xFFFFFFFF: no entry), and the
+// escape offset of the chunk that starts inside the segment (for a segment
+// that overlaps two chunks; the entries from there on belong to the second).
+struct Batch {
+    uint32_t pv, mid;
+};
+__device__ __forceinline__ Batch batch_issue(const DecodeArgs& a, uint32_t b, uint32_t hi,
+                                             uint32_t s0, uint32_t s1) {
+    const uint32_t lane = threadIdx.x & 31;
+    Batch e{0xFFFFFFFFu, 0u};
+    if (b < hi && lane < hi - b) {  // not b + lane < hi: the sum may wrap
+        e.pv = (uint32_t)a.esc_pos[b + lane] | ((uint32_t)a.esc_val[b + lane] << 16);
+        const uint32_t ca = chunk_quot32(a.cdiv, s0), cbk = chunk_quot32(a.cdiv, s1 - 1);
+        if (cbk == ca + 1) e.mid = a.chunk_off[cbk];
+    }
+    return e;
+}
+
+// Segment-relative index of batch entry j = b + lane (its values in e), or
+// 0xFFFFFFFF when absent or when its metadata points outside [s0, s1).
+__device__ __forceinline__ uint32_t batch_index(const DecodeArgs& a, const Batch& e, uint32_t j,
+                                                uint32_t s0, uint32_t s1) {
+    if (e.pv == 0xFFFFFFFFu) return 0xFFFFFFFFu;
+    const uint32_t ca = chunk_quot32(a.cdiv, s0), cbk = chunk_quot32(a.cdiv, s1 - 1);
+    const uint32_t c = ca == cbk ? ca
+                       : cbk == ca + 1 ? (j >= e.mid ? cbk : ca)
+                                       : chunk_of_entry(a, j, ca, cbk);
+    const uint32_t pos = e.pv & 0xFFFFu;
+    const uint32_t x = c * a.cdiv.d + pos;
+    return (pos < a.cdiv.d && x >= s0 && x < s1) ? x - s0 : 0xFFFFFFFFu;
+}
+
+// Writes the escapes [lo, hi) of segment [s0, s1) over their output bytes
+// (the first 32 in eb, then further batches).  fields: the segment's staged
+// field bytes, or null to read them from the field stream.
+__device__ __forceinline__ void patch(const DecodeArgs& a, const Batch& eb, uint32_t lo,
+                                      uint32_t hi, uint32_t s0, uint32_t s1, const uint8_t* fields) {
+    const uint32_t lane = threadIdx.x & 31;
+    auto put = [&](const Batch& e, uint32_t b) {
+        const uint32_t local = batch_index(a, e, b + lane, s0, s1);
+        if (local != 0xFFFFFFFFu) {
+            const uint32_t f = fields ? field_at(fields, local) : field_at(a.signman, (uint64_t)s0 + local);
+            a.y[s0 + local] = (uint8_t)(((f & 4u) << 5) | (((e.pv >> 16) << 2) & 0x7Cu) | (f & 3u));
+        }
+    };
+    put(eb, lo);
+    for (uint32_t b = lo; hi - b > 32;) {  // lo <= b < hi; no sum that could wrap
+        b += 32;
+        put(batch_issue(a, b, hi, s0, s1), b);
+    }
+}
+
+// The dense words of group k of a segment not staged (the last, partial one),
+// straight from global memory; bytes past s1 read as 0.
+__device__ __forceinline__ void load_partial(const DecodeArgs& a, uint32_t s0, uint32_t s1,
+                                             uint32_t i, uint4& c, uint32_t (&w)[3]) {
+    (void)s0;
+    uint32_t cw[4] = {0, 0, 0, 0};
+    w[0] = w[1] = w[2] = 0;
+    const uint8_t* smp = a.signman + (uint64_t)(i / 32) * 12;
+    if (i < s1) {
+        const uint32_t rem = s1 - i < 32 ? s1 - i : 32;
+        const uint32_t nc = (rem + 1) / 2, ns = (3 * rem + 7) / 8;
 #pragma unroll
-        for (int k = 0; k < kGroups; k++) {
-            const uint32_t i = s0 + 1024 * k + 32 * lane;
-            const uint8_t* smp = a.signman + (uint64_t)(i / 32) * 12;
-            if (full || (uint64_t)i + 32 <= s1) {
-                d.code[k] = ld_stream16(a.codes + i / 2);
-                d.smw[k][0] = ld_stream4(smp);
-                d.smw[k][1] = ld_stream4(smp + 4);
-                d.smw[k][2] = ld_stream4(smp + 8);
-            } else {
-                uint32_t cw[4] = {0, 0, 0, 0};
-                d.smw[k][0] = d.smw[k][1] = d.smw[k][2] = 0;
-                if (i < s1) {
-                    const uint32_t rem = s1 - i;
-                    for (uint32_t j = 0; j < (rem + 1) / 2; j++)
-                        cw[j >> 2] |= (uint32_t)a.codes[i / 2 + j] << (8 * (j & 3));
-                    for (uint32_t j = 0; j < (3 * rem + 7) / 8; j++)
-                        d.smw[k][j >> 2] |= (uint32_t)smp[j] << (8 * (j & 3));
+        for (int j = 0; j < 16; j++)
+            if ((uint32_t)j < nc) cw[j >> 2] |= (uint32_t)a.codes[i / 2 + j] << (8 * (j & 3));
+#pragma unroll
+        for (int j = 0; j < 12; j++)
+            if ((uint32_t)j < ns) w[j >> 2] |= (uint32_t)smp[j] << (8 * (j & 3));
+    }
+    c = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+}
+
+}  // namespace e5
+
+__global__ void __launch_bounds__(kThreads, e5::kMinBlocks) decode_e5m2_kernel(const DecodeArgs a) {
+    using namespace e5;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint32_t cb[4];  // the codebook, each entry shifted into the exponent field
+    {
+        uint32_t cbw[4];
+        codebook_words(a.dcb, a.cbw, cbw);
+#pragma unroll
+        for (int q = 0; q < 4; q++) cb[q] = (cbw[q] << 2) & 0x7C7C7C7Cu;
+    }
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t warps = gridDim.x * kWarps;
+    const uint32_t nseg = (uint32_t)(((uint64_t)a.n + kSeg - 1) / kSeg);  // n may be 2^32 - 1
+    const uint32_t full_segs = a.n / (uint32_t)kSeg;
+    uint8_t* ring = smem + (size_t)warp * kStageBytes;  // stage st at ring + st * kWarps * kStageBytes
+    uint32_t seg = blockIdx.x * kWarps + warp;
+    if (seg >= nseg) return;  // warp-uniform
+    const uint64_t pol = l2_evict_first_policy();  // the streams are read once
+
+    // Lanes copy the segment's dense bytes 16 at a time; a lane reads bytes
+    // other lanes copied, so every read of a stage follows this lane's wait
+    // and a __syncwarp, and every refill follows a __syncwarp after the reads.
+    auto fill = [&](uint32_t sg, int st) {
+        if (sg < full_segs) {
+            const uint32_t s0 = sg * (uint32_t)kSeg;
+            uint8_t* dst = ring + (size_t)st * kWarps * kStageBytes;
+#pragma unroll
+            for (uint32_t q = 0; q < (kPieces + 31) / 32; q++) {
+                const uint32_t piece = q * 32 + lane;
+                if (piece < (uint32_t)kPieces) {
+                    const uint32_t off = piece * 16;
+                    const uint8_t* src = off < (uint32_t)kCodeBytes
+                                             ? a.codes + s0 / 2 + off
+                                             : a.signman + (uint64_t)(s0 / 8) * 3 + (off - kCodeBytes);
+                    cp_async16_hint(dst + off, src, pol);
                 }
-                d.code[k] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
             }
         }
-        return d;
-    }
-    // Exponents enter the words already shifted to bits 2..6 of the byte.
-    static constexpr bool kPairs = false;  // exponents from the codebook registers
-    static constexpr int kMinBlocks = 5;  // resident CTAs per SM: 48 registers, 1.4% faster than 4
-    static __device__ __forceinline__ uint32_t exp_byte(uint32_t e) { return (e << 2) & 0x7Cu; }
-    static __device__ __forceinline__ void decode(const Luts& lut, const Dense& d, Ex& ex) {
+        cp_async_commit();  // one group per segment, empty when not staged
+    };
+
 #pragma unroll
-        for (int k = 0; k < kGroups; k++) {
-            const uint32_t cw[4] = {d.code[k].x, d.code[k].y, d.code[k].z, d.code[k].w};
-#pragma unroll
-            for (int i = 0; i < 4; i++) cb_lookup8(lut.cb, cw[i], ex.e[8 * k + 2 * i], ex.e[8 * k + 2 * i + 1]);
+    for (int st = 0; st < kStages; st++) fill(seg + st * warps, st);
+    Slice cur = slice_finish(a, slice_issue(a, seg, nseg));
+    Slice nxt = slice_issue(a, seg + warps, nseg);  // finished an iteration later
+    Batch eb = batch_issue(a, cur.lo, cur.hi, seg * (uint32_t)kSeg,
+                           a.n - seg * (uint32_t)kSeg < (uint32_t)kSeg ? a.n : seg * (uint32_t)kSeg + kSeg);
+    int stage = 0;
+    while (true) {
+        const uint32_t s0 = seg * (uint32_t)kSeg;
+        const uint32_t s1 = a.n - s0 < (uint32_t)kSeg ? a.n : s0 + kSeg;
+        const uint32_t next = seg + warps;
+        const bool more = next < nseg;
+        const Slice nxt2 = slice_issue(a, next + warps, nseg);  // two segments ahead
+        nxt = slice_finish(a, nxt);
+        Batch ebn{0xFFFFFFFFu, 0u};
+        if (more) {
+            const uint32_t n0 = next * (uint32_t)kSeg;
+            ebn = batch_issue(a, nxt.lo, nxt.hi, n0, a.n - n0 < (uint32_t)kSeg ? a.n : n0 + kSeg);
         }
-    }
-    static __device__ __forceinline__ void locate(uint32_t local, uint32_t& q, uint32_t& l,
-                                                  uint32_t& byte) {
-        q = 8 * (local >> 10) + ((local >> 2) & 7u);
-        l = (local >> 5) & 31u;
-        byte = local & 3u;
-    }
-    static __device__ __forceinline__ void store(const DecodeArgs& a, uint32_t s0, uint32_t s1,
-                                                 uint32_t lane, const Dense& d, const Ex& ex) {
-        const bool full = s1 - s0 == (uint32_t)kSeg;
+        const uint8_t* st_base = ring + (size_t)stage * kWarps * kStageBytes;
+        const bool staged = seg < full_segs;  // warp-uniform
+        if (staged) {
+            cp_async_wait<kStages - 1>();  // this segment's group (the oldest pending) has landed
+            __syncwarp();
 #pragma unroll
-        for (int k = 0; k < kGroups; k++) {
-            const uint32_t i = s0 + 1024 * k + 32 * lane;
-            if (!full && i >= s1) continue;
-            const uint32_t w0 = d.smw[k][0], w1 = d.smw[k][1], w2 = d.smw[k][2];
-            const uint32_t f12[8] = {
-                w0 & 0xFFFu, (w0 >> 12) & 0xFFFu, __funnelshift_r(w0, w1, 24) & 0xFFFu,
-                (w1 >> 4) & 0xFFFu, (w1 >> 16) & 0xFFFu, __funnelshift_r(w1, w2, 28) & 0xFFFu,
-                (w2 >> 8) & 0xFFFu, w2 >> 20};
-            uint32_t out[8];
-#pragma unroll
-            for (int m = 0; m < 8; m++) out[m] = assemble_e5m2(f12[m], ex.e[8 * k + m]);
-            if (full) {
+            for (int k = 0; k < 2; k++) {
+                const uint4 c = *reinterpret_cast<const uint4*>(st_base + 512 * k + 16 * lane);
+                const uint32_t* w =
+                    reinterpret_cast<const uint32_t*>(st_base + kCodeBytes + 384 * k + 12 * lane);
+                uint32_t out[8];
+                group(cb, c, w[0], w[1], w[2], out);
                 uint8_t* yb = a.y + (s0 + 32 * lane) + 1024 * k;
                 st_stream16(yb, make_uint4(out[0], out[1], out[2], out[3]));
                 st_stream16(yb + 16, make_uint4(out[4], out[5], out[6], out[7]));
-            } else if (s1 - i >= 32) {  // i < s1 here
-                st_stream16(a.y + i, make_uint4(out[0], out[1], out[2], out[3]));
-                st_stream16(a.y + i + 16, make_uint4(out[4], out[5], out[6], out[7]));
-            } else {
-                for (uint32_t j = 0; j < s1 - i; j++) a.y[i + j] = (uint8_t)(out[j >> 2] >> (8 * (j & 3)));
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 2; k++) {
+                const uint32_t i = s0 + 1024 * k + 32 * lane;
+                uint4 c;
+                uint32_t w[3];
+                load_partial(a, s0, s1, i, c, w);
+                uint32_t out[8];
+                group(cb, c, w[0], w[1], w[2], out);
+                if (i < s1) {
+                    if (s1 - i >= 32) {
+                        st_stream16(a.y + i, make_uint4(out[0], out[1], out[2], out[3]));
+                        st_stream16(a.y + i + 16, make_uint4(out[4], out[5], out[6], out[7]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++)
+                            if ((uint32_t)j < s1 - i) a.y[i + j] = (uint8_t)(out[j >> 2] >> (8 * (j & 3)));
+                    }
+                }
             }
         }
+        if (cur.lo < cur.hi) {  // warp-uniform
+            __syncwarp();  // the word stores of every lane come before the escape bytes
+            patch(a, eb, cur.lo, cur.hi, s0, s1, staged ? st_base + kCodeBytes : nullptr);
+        }
+        __syncwarp();  // every lane has read the stage before it is refilled
+        fill(seg + kStages * warps, stage);
+        stage = stage + 1 == kStages ? 0 : stage + 1;
+        if (!more) break;
+        seg = next;
+        cur = nxt;
+        nxt = nxt2;
+        eb = ebn;
     }
-};
+    cp_async_wait<0>();
+}
 
 template <class F>
 __global__ void __launch_bounds__(kThreads, F::kMinBlocks) decode_kernel(const DecodeArgs a) {
@@ -570,37 +645,34 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) decode_kernel(const D
     lut.pairs = pairs;
     uint32_t cbw[4];
     codebook_words(a.dcb, a.cbw, cbw);
-    if constexpr (F::kPairs) build_pairs<F>(pairs, cbw);
-#pragma unroll
-    for (int q = 0; q < 4; q++) {  // F::exp_byte of each byte of the codebook words
-        const uint32_t w = cbw[q];
-        lut.cb[q] = F::exp_byte(w & 0xFFu) | (F::exp_byte((w >> 8) & 0xFFu) << 8) |
-                    (F::exp_byte((w >> 16) & 0xFFu) << 16) | (F::exp_byte(w >> 24) << 24);
-    }
-    if constexpr (F::kRing) decode_segments<F>(a, smem, lut);
-    else decode_segments_regs<F>(a, smem, lut);
+    build_pairs<F>(pairs, cbw);
+    decode_segments_regs<F>(a, smem, lut);
 }
 
-template <class F>
-cudaError_t launch_segments(const DecodeArgs& a, cudaStream_t s) {
-    constexpr size_t smem = decode_smem_bytes<F>();
+// One resident wave of CTAs of kernel K (grid-stride over the segments).
+template <auto K>
+cudaError_t launch_segment_wave(const DecodeArgs& a, uint32_t seg_elems, size_t smem,
+                                cudaStream_t s) {
     Wave wv;
-    const cudaError_t e = launch_wave<decode_kernel<F>>(kThreads, smem, wv);
+    const cudaError_t e = launch_wave<K>(kThreads, smem, wv);
     if (e != cudaSuccess) return e;
-    const uint64_t nseg = ((uint64_t)a.n + F::kSeg - 1) / F::kSeg;
+    const uint64_t nseg = ((uint64_t)a.n + seg_elems - 1) / seg_elems;
     const uint64_t ctas = (nseg + kWarps - 1) / kWarps;
     const uint64_t wave = wv.ctas();
-    decode_kernel<F><<<(uint32_t)(ctas < wave ? ctas : wave), kThreads, smem, s>>>(a);
+    K<<<(uint32_t)(ctas < wave ? ctas : wave), kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_tile_elems(bool e5m2) { return (e5m2 ? E5m2Seg::kSeg : Bf16Seg::kSeg) * kWarps; }
+int decode_tile_elems(bool e5m2) { return (e5m2 ? e5::kSeg : Bf16Seg::kSeg) * kWarps; }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool e5m2, cudaStream_t s) {
     if (a.n == 0) return cudaSuccess;
-    return e5m2 ? launch_segments<E5m2Seg>(a, s) : launch_segments<Bf16Seg>(a, s);
+    if (e5m2)
+        return launch_segment_wave<decode_e5m2_kernel>(
+            a, e5::kSeg, (size_t)e5::kStages * kWarps * e5::kStageBytes, s);
+    return launch_segment_wave<decode_kernel<Bf16Seg>>(a, Bf16Seg::kSeg, decode_smem_bytes<Bf16Seg>(), s);
 }
 
 }  // namespace splitzip
