@@ -244,14 +244,18 @@ splitzip_status splitzip_decode_devcb_e5m2(const splitzip_streams *in, uint64_t 
  * exceed SPLITZIP_NOALLOC_MAX_ELEMENTS (SPLITZIP_ERR_TOO_LARGE otherwise).
  * Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call shares the one array, which keeps the last call's
- * contents; each call clears what must start at zero, but calls that overlap
- * on the GPU (different streams or threads) race and must not be issued.
+ * device, with that device current, and once more after the device's context
+ * has been reset, e.g. by cudaDeviceReset, since the array may then sit
+ * elsewhere); make that first call before any stream capture.  Every call
+ * shares the one array, which keeps the last call's contents; each call clears
+ * what must start at zero, but calls that overlap on the GPU (different
+ * streams or threads) race and must not be issued.
  * d_status_out (4-byte aligned device memory, may be NULL) receives the
  * device-side status bits of this encode once it finishes: 0 = success,
  * bit 0 (1) = escape overflow (E > esc_capacity), bit 1 (2) = a bounded wait
- * gave up (streams invalid).  E is chunk_off[C], as for splitzip_encode. */
+ * gave up (streams invalid), bit 2 (4) = the encode found its scratch state
+ * inconsistent (streams invalid; the next call starts clean again).  E is
+ * chunk_off[C], as for splitzip_encode. */
 splitzip_status splitzip_encode_noalloc(const void *d_x, uint64_t n, uint32_t chunk_size,
                                         const splitzip_codebook *cb,
                                         const splitzip_streams *out, uint32_t *d_status_out,

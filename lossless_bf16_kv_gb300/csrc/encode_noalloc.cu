@@ -16,6 +16,8 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>  // driver types only: the two driver calls are reached through the runtime
+
 #include "../../include/splitzip.h"
 #include "kernels.h"
 
@@ -30,24 +32,58 @@ constexpr size_t kNoAllocScratchBytes = kWsHeaderBytes + 8 * kNoAllocTiles;
 // Every GPU that loads the library holds this array (about 2 MiB) until exit.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Id of the context current on this thread (0 if none is, or if the driver
+// does not offer the calls).  The array's device address belongs to one
+// context: a device reset makes a new one, in which the array may sit
+// elsewhere, so the cached address is keyed on the context's id.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 constexpr int kMaxDevices = 128;
 std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};
 
 // Device address of the array on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is fetched once
-// per device, with that device current, and cached.
+// per device (and again after a device reset), with that device current, and
+// cached.
 cudaError_t scratch_on_current_device(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> g(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // binds the device's context
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = current_context_id();
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;

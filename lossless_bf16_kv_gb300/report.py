@@ -31,7 +31,8 @@ TOPK = (1, 2, 4, 8, 16)
 
 def exponent_stats(hist, codebook, fmt: str = "bf16", chunk: int = 1024) -> dict:
     """Statistics of one exponent histogram (256 BF16 / 32 E5M2 bins) under a
-    codebook (16 exponents, as splitzip_calibrate returns it)."""
+    codebook (16 exponents, as splitzip_calibrate returns it).  Sizes come from
+    the library's closed forms (pure host functions, no GPU needed)."""
     h = np.asarray(hist, dtype=np.int64)
     n = int(h.sum())
     if n == 0:
@@ -40,14 +41,13 @@ def exponent_stats(hist, codebook, fmt: str = "bf16", chunk: int = 1024) -> dict
     entropy = float(-(p * np.log2(p)).sum())
     ranked = np.sort(h)[::-1]
     cover = {k: float(ranked[:k].sum() / n) for k in TOPK}
+    from . import splitzip as sz
     cb = [int(c) for c in codebook]
     covered = int(h[cb].sum())
     escapes = n - covered
     elem = 2 if fmt == "bf16" else 1
-    sm = n if fmt == "bf16" else (3 * n + 7) // 8
-    chunks = -(-n // chunk)
-    compressed = (n + 1) // 2 + sm + 3 * escapes + 4 * (chunks + 1)
-    entropy_bytes = math.ceil(n * entropy / 8) + sm
+    compressed = sz.splitzip_compressed_bytes(n, chunk, escapes, fmt)
+    entropy_bytes = math.ceil(n * entropy / 8) + sz.splitzip_signman_bytes(n, fmt)
     return {"fmt": fmt, "n": n, "entropy_bits": entropy, "distinct_exponents": int((h > 0).sum()),
             "topk_coverage": cover, "codebook": [int(c) for c in cb], "escape_rate": escapes / n,
             "n_escapes": escapes, "compression_ratio": n * elem / compressed,

@@ -180,7 +180,7 @@ def _elements(x: torch.Tensor, fmt: str, what: str = "x") -> int:
 
 
 def _need_streams(s: dict, n: int, chunk: int, fmt: str):
-    _need(s["codes"], (n + 1) // 2, "codes")
+    _need(s["codes"], splitzip_codes_bytes(n), "codes")
     _need(s["signman"], splitzip_signman_bytes(n, fmt), "signman")
     _need(s["chunk_off"], 4 * (splitzip_num_chunks(n, chunk) + 1), "chunk_off")
 
@@ -217,6 +217,10 @@ def splitzip_num_chunks(n: int, chunk: int) -> int:
     return int(library().splitzip_num_chunks(n, chunk))
 
 
+def splitzip_codes_bytes(n: int) -> int:
+    return int(library().splitzip_codes_bytes(n))
+
+
 def splitzip_signman_bytes(n: int, fmt: str = "bf16") -> int:
     lib = library()
     return int(lib.splitzip_signman_bytes(n) if fmt == "bf16" else lib.splitzip_signman_bytes_e5m2(n))
@@ -238,7 +242,7 @@ def alloc_streams(n: int, chunk: int, fmt: str = "bf16", esc_capacity: int | Non
     """Empty stream buffers for n elements (esc_capacity defaults to n // 32 + 1024)."""
     cap = n // 32 + 1024 if esc_capacity is None else esc_capacity
     return {
-        "codes": torch.empty((n + 1) // 2, dtype=torch.uint8, device=device),
+        "codes": torch.empty(splitzip_codes_bytes(n), dtype=torch.uint8, device=device),
         "signman": torch.empty(splitzip_signman_bytes(n, fmt), dtype=torch.uint8, device=device),
         "esc_pos": torch.empty(cap, dtype=torch.int16, device=device),
         "esc_val": torch.empty(cap, dtype=torch.uint8, device=device),
@@ -543,7 +547,7 @@ class Encoded:
 
     @property
     def compressed_bytes(self) -> int:
-        """ceil(n/2) + sign/mantissa bytes + 3E + 4(C+1) (codebook not counted)."""
+        """Compressed size from the library's closed form (codebook not counted)."""
         return splitzip_compressed_bytes(self.n, self.chunk, self.n_escapes, self.fmt)
 
     @property

@@ -1,7 +1,8 @@
-"""The C ABI used from plain C: tests/c_abi_roundtrip.c includes only
-include/splitzip.h and the CUDA runtime and links libsplitzip.so.  On CPU the
-program must compile and link; on a GPU its codebook and streams must be the
-oracle's, byte for byte, and its decode bit-exact."""
+"""The C ABI used from plain C: tests/c_abi_roundtrip.c (and
+tests/c_noalloc_reset.c, run by the no-allocation tests) include only
+include/splitzip.h and the CUDA runtime and link libsplitzip.so.  On CPU the
+programs must compile and link; on a GPU the round trip's codebook and streams
+must be the oracle's, byte for byte, and its decode bit-exact."""
 import glob
 import os
 import subprocess
@@ -23,21 +24,22 @@ def _cuda_dirs():
     return os.path.join(root, "include"), libs[0]
 
 
-def compile_program(out_dir) -> str:
+def compile_program(out_dir, src: str = SRC) -> str:
     _build.build_library()
     inc, cudalib = _cuda_dirs()
-    exe = os.path.join(str(out_dir), "c_abi_roundtrip")
+    exe = os.path.join(str(out_dir), os.path.basename(src)[:-2])
     libdir = os.path.dirname(_build.LIBPATH)
     cmd = ["gcc", "-std=c99", "-O2", "-Wall", "-Wextra", "-Werror", f"-I{ROOT}/include", f"-I{inc}",
-           SRC, "-o", exe, f"-L{libdir}", "-lsplitzip", f"-L{cudalib}", "-lcudart",
+           src, "-o", exe, f"-L{libdir}", "-lsplitzip", f"-L{cudalib}", "-lcudart",
            f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{cudalib}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     return exe
 
 
-def test_c_program_compiles_against_the_header(tmp_path):
-    exe = compile_program(tmp_path)
+@pytest.mark.parametrize("name", ["c_abi_roundtrip.c", "c_noalloc_reset.c"])
+def test_c_program_compiles_against_the_header(tmp_path, name):
+    exe = compile_program(tmp_path, os.path.join(ROOT, "tests", name))
     assert os.access(exe, os.X_OK)
 
 
