@@ -378,20 +378,15 @@ __device__ __forceinline__ uint32_t sel(uint32_t a, uint32_t b, uint32_t m) {
     return (a & m) | (b & ~m);
 }
 
-// One output word (four E5M2 values).  lo: the word's four 3-bit fields at
-// bits 0..11 of lo, and the same fields at bits 10..21 of hi (other bits of
-// lo and hi are ignored); ea | eb: the four exponents in place.  The fields
-// are spread to the bottom of each byte in two select steps (f0, f1 stay,
-// f2, f3 move up 10; then f1, f3 move up 5), the sign bits move to bit 7.
-__device__ __forceinline__ uint32_t word(uint32_t lo, uint32_t hi, uint32_t ea, uint32_t eb) {
-    const uint32_t t = sel(hi, lo, 0xFFFF0000u);       // f0 f1 at 0..5, f2 f3 at 16..21
-    const uint32_t f = sel(t << 5, t, 0x07000700u);    // field j at bits 8j..8j+2
-    const uint32_t u = sel(f << 5, f, 0x80808080u);    // sign bit of byte j at 8j+7
-    return ((u & 0x83838383u) | ea) | eb;
-}
-
 // The eight output words of a group: codes c (16 bytes), fields w0..w2
 // (12 bytes, field j at bits 3j..3j+2 of the 96-bit little-endian stream).
+// Fields are spread eight at a time: a 24-bit run of eight fields is split
+// into two 12-bit halves 16 bits apart, each half into two 6-bit pairs 8 bits
+// apart; the even and odd fields of the pairs are masked out and interleaved
+// byte by byte with permutes.  Multiplying a byte holding sign << 2 | mantissa
+// by 33 adds a copy 5 bits up, which puts the sign at bit 7 (no carry between
+// bytes: 7 * 33 < 256); masking keeps bits 7, 1 and 0, and the exponents
+// (bits 2..6) are OR-ed in.
 __device__ __forceinline__ void group(const uint32_t (&cb)[4], const uint4& c, uint32_t w0,
                                       uint32_t w1, uint32_t w2, uint32_t (&out)[8]) {
     uint32_t a[8], b[8];
@@ -399,15 +394,16 @@ __device__ __forceinline__ void group(const uint32_t (&cb)[4], const uint4& c, u
     cb_lookup8(cb, c.y, a[2], b[2], a[3], b[3]);
     cb_lookup8(cb, c.z, a[4], b[4], a[5], b[5]);
     cb_lookup8(cb, c.w, a[6], b[6], a[7], b[7]);
-    // Word m's fields start at stream bit 12 m.
-    out[0] = word(w0, w0 << 10, a[0], b[0]);
-    out[1] = word(w0 >> 12, w0 >> 2, a[1], b[1]);
-    out[2] = word(__funnelshift_r(w0, w1, 24), __funnelshift_r(w0, w1, 14), a[2], b[2]);
-    out[3] = word(w1 >> 4, w1 << 6, a[3], b[3]);
-    out[4] = word(w1 >> 16, w1 >> 6, a[4], b[4]);
-    out[5] = word(__funnelshift_r(w1, w2, 28), __funnelshift_r(w1, w2, 18), a[5], b[5]);
-    out[6] = word(w2 >> 8, w2 << 2, a[6], b[6]);
-    out[7] = word(w2 >> 20, w2 >> 10, a[7], b[7]);
+    const uint32_t v[4] = {w0, __funnelshift_r(w0, w1, 24), __funnelshift_r(w1, w2, 16), w2 >> 8};
+#pragma unroll
+    for (int p = 0; p < 4; p++) {  // fields 8p..8p+7 (bits above the 24th are ignored)
+        const uint32_t h = sel(v[p] << 4, v[p], 0xFFFF0000u);  // fields 4..7 at bits 16..27
+        const uint32_t q = sel(h << 2, h, 0xFF00FF00u);        // pair k at bits 8k..8k+5
+        const uint32_t ev = q & 0x07070707u, od = (q >> 3) & 0x07070707u;
+        const uint32_t x0 = __byte_perm(ev, od, 0x5140), x1 = __byte_perm(ev, od, 0x7362);
+        out[2 * p] = ((x0 * 33u) & 0x83838383u) | a[2 * p] | b[2 * p];
+        out[2 * p + 1] = ((x1 * 33u) & 0x83838383u) | a[2 * p + 1] | b[2 * p + 1];
+    }
 }
 
 // The 3-bit field of element j of a field stream f of `bytes` bytes.
