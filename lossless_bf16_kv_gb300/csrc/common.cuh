@@ -29,7 +29,9 @@ struct WsHeader {
     uint64_t last_escapes;  // encode: E of the last finished launch
     uint64_t cal_covered;   // calibrate: covered count (synchronous API readback)
     uint8_t cal_cb[16];     // calibrate: codebook (synchronous API readback)
-    uint64_t reserved[24];
+    uint32_t dense_next;    // encode: next tile handed to a CTA of the dense pass
+    uint32_t dense_done;    // encode: tiles the dense pass has processed
+    uint64_t reserved[23];
     unsigned long long hist[256];  // calibrate: global exponent histogram, zero between launches
 };
 static_assert(sizeof(WsHeader) <= 4096, "header must fit its slot");

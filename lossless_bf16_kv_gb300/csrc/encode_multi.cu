@@ -530,14 +530,17 @@ struct E5m2Dense {
 
 // --------------------------------------------------------------- K1 dense
 
-// Grid-stride over tiles (one resident wave): the code table is built once
-// per CTA and the tile loop has no barrier at all.  The input of full tiles
-// comes through a per-thread ring of kDenseStages shared-memory slots filled
-// by cp.async: while a thread works on one tile, its copies of the next
-// kDenseStages - 1 tiles are in flight, with no registers held for them.
-// Each thread reads back only the bytes it copied itself, so waiting for its
-// own copy groups is all the synchronisation needed.  A slot is refilled only
-// after the values read from it have been used by the tile's stores.
+// One resident wave of CTAs; the code table is built once per CTA.  Tiles
+// are handed out one at a time from a counter in the workspace header (in
+// increasing order across the GPU), so CTAs that run faster take more tiles:
+// with a static split, CTAs of equal work finished up to three times apart.
+// Thread 0 draws the id of the tile two iterations ahead while the CTA works
+// on the current one; one CTA barrier per tile publishes it.  The input of
+// full tiles comes through a per-thread ring of kDenseStages shared-memory
+// slots filled by cp.async: while a thread works on one tile, its copies of
+// the next kDenseStages - 1 tiles are in flight, with no registers held for
+// them.  A slot is refilled only after the values read from it have been used
+// by the tile's stores.
 constexpr int kDenseStages = 2;
 
 template <class F>
@@ -549,12 +552,16 @@ template <class F>
 __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const EncodeArgs a,
                                                                        const MultiPtrs p) {
     constexpr int L = F::kLoads, S = kDenseStages;
+    static_assert(kDenseStages == 2, "two tile ids ahead");
     extern __shared__ uint4 ring[];  // [S][L][kThreads]
     __shared__ typename F::Tables tables;
+    __shared__ uint32_t s_grab[3];   // tile ids drawn by thread 0: [0..1] alternate, [2] the first pair
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+    if (threadIdx.x == 0) s_grab[2] = atomicAdd(&hdr->dense_next, (uint32_t)S);
     {
         uint32_t cbw[4];
         codebook_words(a.dcb, a.cbw, cbw);
-        F::build_tables(tables, cbw);
+        F::build_tables(tables, cbw);  // ends with a CTA barrier: s_grab[2] is visible
     }
     // With F::kKeepLists, counts and list entries stay in L2 for the prefix and
     // placement passes while the tensor streams through.
@@ -569,10 +576,13 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
         }
         cp_async_commit();  // one group per tile, empty for a tile not staged
     };
-#pragma unroll
-    for (int s = 0; s < S; s++) fill(blockIdx.x + s * gridDim.x, s);
+    uint32_t tile = s_grab[2], next = tile + 1;
+    fill(tile, 0);
+    fill(next, 1);
     int slot = 0;
-    for (uint32_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+    uint32_t it = 0;
+    for (; tile < a.num_tiles; it++) {
+        if (threadIdx.x == 0) s_grab[it & 1] = atomicAdd(&hdr->dense_next, 1u);  // two ahead
         const uint32_t t0 = tile * (uint32_t)kTileElems;
         typename F::Keep kp;
         const uint8_t* in;  // the tile's input, from which the escapes are read
@@ -593,11 +603,15 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
         } else {
             F::bookkeep_multi(kp, row, ent, in, keep);
         }
-        if (F::kSharedStage) __syncwarp();  // every lane has read the stage before the refill
-        fill(tile + S * gridDim.x, slot);
+        __syncthreads();  // the drawn id is visible; every lane has read the stage
+        const uint32_t ahead = s_grab[it & 1];
+        fill(ahead, slot);
         slot = slot + 1 == S ? 0 : slot + 1;
+        tile = next;
+        next = ahead;
     }
     cp_async_wait<0>();
+    if (threadIdx.x == 0 && it) atomicAdd(&hdr->dense_done, it);  // tiles this CTA processed
 }
 
 // -------------------------------------------------------------- K2 prefix
@@ -612,11 +626,16 @@ __device__ void prefix_finished(const EncodeArgs& a, uint32_t epoch) {
     if (prev == gridDim.x - 1) {
         __threadfence();
         const uint32_t tickets = atomicAdd(&hdr->ticket, 0u);
+        const uint32_t dense_done = atomicAdd(&hdr->dense_done, 0u);
         const bool timed_out = (atomicAdd(&hdr->status, 0u) & kStatusTimeout) != 0;
-        if (!timed_out && tickets != gridDim.x) atomicOr(&hdr->status, kStatusBadWorkspace);
+        // Every tile processed exactly once, every prefix CTA drew one ticket.
+        if (!timed_out && (tickets != gridDim.x || dense_done != a.num_tiles))
+            atomicOr(&hdr->status, kStatusBadWorkspace);
         hdr->last_status = atomicExch(&hdr->status, 0u);
         hdr->ticket = 0;
         hdr->done = 0;
+        hdr->dense_next = 0;
+        hdr->dense_done = 0;
         hdr->epoch = epoch + 1u;
         __threadfence();
     }
