@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 # roofline is taken per call: algorithmic bytes of the call over its time.
 KERNELS = {"encode": ("encode[dense_kernel+prefix_kernel+place_kernel]<Bf16Dense>",
                       "encode[dense_kernel+prefix_kernel+place_kernel]<E5m2Dense>"),
-           "decode": ("decode_kernel<Bf16Seg>", "decode_kernel<E5m2Seg>")}
+           "decode": ("decode_kernel<Bf16Seg>", "decode_e5m2_kernel")}
 
 
 # ------------------------------------------------------------ host helpers
