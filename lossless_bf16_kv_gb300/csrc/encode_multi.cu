@@ -749,6 +749,70 @@ __device__ __forceinline__ bool in_codebook(const uint32_t (&cbw)[4], uint32_t e
     return z != 0;
 }
 
+// The escapes of segment sg (element order) of tile `tile`, rebuilt from the
+// input by the whole warp: a segment whose escapes did not all fit in its
+// warp's list (escape-heavy data).  Lane j takes the segment's elements
+// j * PER .. j * PER + PER - 1 (one or two 16-byte loads), flags its escapes
+// through the shared-memory table isesc (1 for an exponent outside the
+// codebook), and stores them from g0 + (the escapes of the lower lanes) on, in
+// element order.  All lanes call it.
+template <class F>
+__device__ __forceinline__ void rebuild_segment(const EncodeArgs& a, uint32_t tile, uint32_t sg,
+                                                uint32_t g0, const uint8_t* isesc) {
+    constexpr uint32_t PER = F::kSegLen / 32;  // 8 BF16 or 32 E5M2 elements per lane
+    constexpr uint32_t W = PER * F::kElemBytes / 4;  // input words per lane: 4 or 8
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t t0 = tile * (uint32_t)kTileElems;
+    const uint32_t len = a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
+    const uint32_t l0 = sg * F::kSegLen + lane * PER;  // the lane's first element, tile-local
+    const uint8_t* src = a.x + (size_t)(t0 + l0) * F::kElemBytes;
+    uint32_t w[W];
+    if (l0 + PER <= len) {
+#pragma unroll
+        for (uint32_t q = 0; q < W; q += 4) {
+            const uint4 v = ld_stream16(src + 4 * q);
+            w[q] = v.x; w[q + 1] = v.y; w[q + 2] = v.z; w[q + 3] = v.w;
+        }
+    } else {  // the segment ends inside this lane's elements (or before them)
+#pragma unroll
+        for (uint32_t q = 0; q < W; q++) {
+            uint32_t acc = 0;
+#pragma unroll
+            for (uint32_t b = 0; b < 4; b++)
+                if (l0 * F::kElemBytes + 4 * q + b < len * F::kElemBytes)
+                    acc |= (uint32_t)src[4 * q + b] << (8 * b);
+            w[q] = acc;
+        }
+    }
+    // Exponent of the lane's element k (k < PER).
+    auto exponent = [&](uint32_t k) {
+        if constexpr (PER == 8) {
+            uint32_t v = w[0];
+#pragma unroll
+            for (uint32_t q = 1; q < W; q++) v = (k >> 1) == q ? w[q] : v;
+            return ((v >> (16 * (k & 1u) + 7)) & 0xFFu);
+        } else {
+            uint32_t v = w[0];
+#pragma unroll
+            for (uint32_t q = 1; q < W; q++) v = (k >> 2) == q ? w[q] : v;
+            return ((v >> (8 * (k & 3u) + 2)) & 0x1Fu);
+        }
+    };
+    uint32_t mask = 0;
+#pragma unroll
+    for (uint32_t k = 0; k < PER; k++)
+        if (l0 + k < len && isesc[exponent(k)]) mask |= 1u << k;
+    uint32_t excl, e31, p31;
+    warp_scan_excl(__popc(mask), excl, e31, p31);
+    uint32_t g = g0 + excl;
+    const uint32_t r0 = t0 - chunk_quot32(a.cdiv, t0) * a.cdiv.d;  // the tile's start in its chunk
+    for (uint32_t m = mask; m; m &= m - 1) {
+        const uint32_t k = __ffs(m) - 1;
+        const uint32_t x = r0 + l0 + k;  // < d + kTileElems, in chunk_quot's exact range
+        put_escape(a, g++, x - chunk_quot(a.cdiv, x) * a.cdiv.d, exponent(k));
+    }
+}
+
 // A warp places the escapes of F::kPlaceRounds x 32 / kSegs consecutive tiles
 // (BF16: 4 x 1, E5M2: 2 x 4): in round r lane l takes segment l mod kSegs
 // (element order) of tile tile0 + r * 32 / kSegs + l / kSegs.  Every round's
@@ -756,13 +820,15 @@ __device__ __forceinline__ bool in_codebook(const uint32_t (&cbw)[4], uint32_t e
 // first F::kPreload entries before any escape is stored (loads cannot pass
 // the stores, which the compiler must assume may alias them), so a warp waits
 // for two memory round trips in all rather than two per tile.
-template <class F>
+template <class F, int R>
 __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, const MultiPtrs p,
                                                             uint32_t num_tiles) {
     constexpr uint32_t kOffMask = (1u << F::kOffBits) - 1u;
     constexpr uint32_t SEGS = F::kSegs, TPW = 32 / F::kSegs;
-    constexpr int R = F::kPlaceRounds, K = F::kPreload;
+    constexpr int K = F::kPreload;
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ uint8_t isesc_all[kWarps][256];  // per warp: 1 for an exponent outside the codebook
+    uint8_t* isesc = isesc_all[warp];
     const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW * R;
     if (tile0 >= num_tiles) return;  // warp-uniform
     const uint32_t sub = lane / SEGS, sgl = lane % SEGS;  // this lane's tile and segment
@@ -837,20 +903,26 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
                     if ((uint32_t)k < cnt[r]) put(g0 + k, ev[r][k]);
                 for (uint32_t q = K; q < cnt[r]; q++) put(g0 + q, es[q]);
             }
-        } else {
-            // More escapes than the segment's entries: rebuild from the input.
-            uint32_t cbw[4];
-            codebook_words(a.dcb, a.cbw, cbw);
-            const uint32_t len = a.n - t0 < (uint32_t)kTileElems ? a.n - t0 : (uint32_t)kTileElems;
-            const uint32_t end = s0 + F::kSegLen < len ? s0 + F::kSegLen : len;
-            uint32_t g = g0;
-            for (uint32_t l = s0; l < end; l++) {
-                const uint32_t e = F::exponent_at(a, t0 + l);
-                if (!in_codebook(cbw, e)) {
-                    const uint32_t x = r0 + l;
-                    put_escape(a, g++, x - chunk_quot(a.cdiv, x) * a.cdiv.d, e);
-                }
+        }  // else: more escapes than the segment's list entries, rebuilt below
+    }
+    // Segments whose escapes overflowed their lists, rebuilt by the whole warp
+    // one at a time (the warp first builds its escape table).
+    bool table = false;
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        for (uint32_t ov = __ballot_sync(0xFFFFFFFFu, cnt[r] && sbase[r] + cnt[r] > (uint32_t)kWarpCap);
+             ov; ov &= ov - 1) {
+            const uint32_t l = __ffs(ov) - 1;
+            const uint32_t g0 = __shfl_sync(0xFFFFFFFFu, excl[r] + off[r], l);
+            if (!table) {  // warp-uniform
+                uint32_t cbw[4];
+                codebook_words(a.dcb, a.cbw, cbw);
+#pragma unroll
+                for (uint32_t e = lane; e < 256; e += 32) isesc[e] = !in_codebook(cbw, e);
+                __syncwarp();
+                table = true;
             }
+            rebuild_segment<F>(a, tile0 + (uint32_t)r * TPW + l / SEGS, l % SEGS, g0, isesc);
         }
     }
 
@@ -953,8 +1025,16 @@ cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
     prefix_kernel<F::kSegs, F::kExpMask><<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const uint32_t per_cta = kWarps * (32 / F::kSegs) * F::kPlaceRounds;  // tiles per placement CTA
-    place_kernel<F><<<(tiles + per_cta - 1) / per_cta, kThreads, 0, s>>>(a, p, tiles);
+    // Placement takes F::kPlaceRounds rounds of tiles per warp, or one round
+    // when that would leave fewer than two waves of CTAs (smaller tensors:
+    // more, shorter warps; escape-heavy segments are rebuilt warp by warp).
+    constexpr uint32_t kTilesPerRound = kWarps * (32 / F::kSegs);  // per CTA
+    const uint64_t two_waves = 2ull * (uint64_t)(wv.sms > 0 ? wv.sms : 1) * 4;  // 4 CTAs per SM
+    const uint32_t wide = kTilesPerRound * F::kPlaceRounds;
+    if ((tiles + wide - 1) / wide >= two_waves)
+        place_kernel<F, F::kPlaceRounds><<<(tiles + wide - 1) / wide, kThreads, 0, s>>>(a, p, tiles);
+    else
+        place_kernel<F, 1><<<(tiles + kTilesPerRound - 1) / kTilesPerRound, kThreads, 0, s>>>(a, p, tiles);
     return cudaGetLastError();
 }
 
