@@ -92,11 +92,12 @@ typedef struct splitzip_streams {
 /* ---------------------------------------------------------------- sizes */
 
 /* Bytes of device workspace needed by calibrate/encode for n elements, about
- * 0.07 bytes per element (per 8192-element tile: a look-back word, a
- * prefix, 32 segment counts and 256 escape entries; independent of the
- * chunk size today -- the argument is kept for later formats).  The workspace
- * must be zero-filled once after allocation (splitzip_workspace_init); the
- * library keeps it consistent afterwards. */
+ * 0.07 bytes per element (per 8192-element tile: a look-back word, an escape
+ * count, 32 segment counts and 256 escape entries; escape counts per block of
+ * 64 tiles and per superblock of 4096 tiles; independent of the chunk size
+ * today -- the argument is kept for later formats).  The workspace must be
+ * zero-filled once after allocation (splitzip_workspace_init); the library
+ * keeps it consistent afterwards. */
 size_t splitzip_workspace_bytes(uint64_t n, uint32_t chunk_size);
 
 /* Zero-fill `bytes` of workspace on stream s (one cudaMemsetAsync). */
@@ -158,7 +159,7 @@ splitzip_status splitzip_histogram_e5m2(const void* d_x, uint64_t n, uint64_t* d
 
 /* Encode n elements at d_x (16-byte aligned; BF16 or E5M2 bit patterns) with
  * codebook *cb (host memory, copied into the launch) into out's streams
- * (README section Abstract; arXiv abstract).  Three kernel launches, enqueued
+ * (README section Abstract; arXiv abstract).  Two kernel launches, enqueued
  * on s; returns without synchronising.  chunk_size: a multiple of 8 in
  * [8, SPLITZIP_MAX_CHUNK].  1 <= n <= SPLITZIP_MAX_ELEMENTS.
  * If E > esc_capacity, the dense streams and chunk_off are still complete and

@@ -2,17 +2,19 @@
  * splitzip_testing.h -- test controls of the SplitZip library (not for
  * production callers).
  *
- * Both encode engines compute the exclusive prefix of escape counts across
- * tiles with a decoupled look-back (per 8192-element tile in the single-launch
- * pipeline, per block of 2048 tiles in the three-launch encode): a tile waits
- * until its predecessors have published their counts.  Every such wait is bounded; when the bound runs
+ * The single-launch encode pipeline (the engine of splitzip_encode_noalloc)
+ * computes the exclusive prefix of escape counts across 8192-element tiles
+ * with a decoupled look-back: a tile waits until its predecessors have
+ * published their counts.  Every such wait is bounded; when the bound runs
  * out the kernel records SPLITZIP_ERR_TIMEOUT in the workspace, publishes a
  * (wrong) prefix so that later tiles are not held up, keeps every write in
  * bounds and returns, leaving the CUDA context usable.  This entry point lets
  * a test make that wait run out on purpose, with a flag that keeps tile 0
- * from ever publishing, and a small poll limit so the test ends quickly.  The
- * method's pages have no counterpart: it exists only to exercise the error
- * path.
+ * from ever publishing, and a small poll limit so the test ends quickly.  (The
+ * default two-launch encode has no waits: its tile offsets come from counters
+ * the first launch completes before the second starts; the stall flag has no
+ * effect on it.)  The method's pages have no counterpart: this entry point
+ * exists only to exercise the error path.
  */
 #ifndef SPLITZIP_TESTING_H
 #define SPLITZIP_TESTING_H
@@ -23,10 +25,11 @@
 extern "C" {
 #endif
 
-/* Tile 0 never publishes its prefix: every later tile's wait runs out. */
+/* Tile 0 never publishes its prefix: every later tile's wait runs out
+ * (single-launch pipeline only). */
 #define SPLITZIP_TEST_STALL_FIRST_TILE 0x1u
 /* Encode with the single-launch pipeline (the engine of
- * splitzip_encode_noalloc) instead of the three-launch encode. */
+ * splitzip_encode_noalloc) instead of the two-launch encode. */
 #define SPLITZIP_TEST_PIPELINED 0x2u
 
 typedef struct splitzip_encode_test_opts {

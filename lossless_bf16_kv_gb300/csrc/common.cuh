@@ -18,7 +18,8 @@ constexpr int kWarps = kThreads / 32;
 // ----------------------------------------------------------- workspace
 //
 // [0, 4096)      header (below)
-// [4096, ...)    one 64-bit tile-state word per encode tile
+// then           the encode's block and superblock escape counters (fixed size)
+// then           one 64-bit tile-state word per encode tile
 struct WsHeader {
     uint32_t ticket;        // encode: next tile id handed to a starting CTA
     uint32_t done;          // encode: CTAs finished in the running launch
@@ -36,6 +37,14 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) <= 4096, "header must fit its slot");
 constexpr size_t kWsHeaderBytes = 4096;
+// Right after the header, at an offset and of a size that do not depend on
+// the element count (so a workspace reused for other sizes keeps them where
+// the previous call re-armed them): the encode's escape counters per block of
+// 64 tiles and per superblock of 4096 tiles, for up to 2^32 elements.
+constexpr size_t kWsSumsBytes = 4 * ((1ull << 32) / 8192 / 64 + (1ull << 32) / 8192 / 4096);
+static_assert(kWsSumsBytes % 256 == 0, "keeps the regions after it 256-byte aligned");
+// The single-launch pipeline's look-back state words follow.
+constexpr size_t kWsStatesOffset = kWsHeaderBytes + kWsSumsBytes;
 
 constexpr uint32_t kStatusOverflow = 1u;
 constexpr uint32_t kStatusTimeout = 2u;

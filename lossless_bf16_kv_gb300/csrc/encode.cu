@@ -487,7 +487,7 @@ __device__ void compute_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm,
         const bool direct = aggregate > (uint32_t)kListCap;  // uniform
         // Past the scan's barrier every compute thread is done with stage s.
         if (tid == 0) {
-            publish_count(reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes), tile, epoch, aggregate,
+            publish_count(reinterpret_cast<uint64_t*>(a.ws + kWsStatesOffset), tile, epoch, aggregate,
                           (a.test_flags & kTestStallFirstTile) != 0);
             mbar_arrive(&sm.empty[s]);
             sm.slot_tile[k] = tile;
@@ -546,7 +546,7 @@ __device__ void lookback_role(const EncodeArgs& a, EncodeSmem<F::kElemBytes>& sm
         const uint32_t agg = min(sm.slot_agg[k], (uint32_t)kTile);
         const uint32_t q0 = sm.slot_q0[k], r0 = sm.slot_r0[k];
         const bool direct = agg > (uint32_t)kListCap;
-        const uint32_t excl = look_back(reinterpret_cast<uint64_t*>(a.ws + kWsHeaderBytes),
+        const uint32_t excl = look_back(reinterpret_cast<uint64_t*>(a.ws + kWsStatesOffset),
                                         &reinterpret_cast<WsHeader*>(a.ws)->status, tile, epoch, agg,
                                         a.spin_limit);
         if (direct) {

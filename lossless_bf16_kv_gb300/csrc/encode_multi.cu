@@ -1,4 +1,4 @@
-// encode_multi.cu -- SplitZip encode in three launches (BF16 and FP8 E5M2).
+// encode_multi.cu -- SplitZip encode in two launches (BF16 and FP8 E5M2).
 //
 // Method ("SplitZip: Ultra-Fast Lossless KV Compression for Disaggregated LLM
 // Serving", README section Abstract; arXiv abstract on the paper index page):
@@ -9,22 +9,22 @@
 // The only cross-tile dependency of the format is the escape stream's order
 // (chunk, then position) and its offsets.  Here it is taken out of the
 // streaming pass:
-//   K1 dense     grid-stride over 8192-element tiles, no inter-CTA
-//                communication: input staged through a per-thread cp.async
-//                ring, field split, code lookup in shared-memory word tables,
-//                dense code and sign+mantissa stores.  Each warp ranks the
-//                escapes of its segments (ballots when no group holds two
-//                escapes, else one shuffle scan) and stores the segments'
-//                counts and its first 32 escapes, as one list in element order
-//                within each segment, in the workspace.
-//   K2 prefix    exclusive prefix of the per-tile escape counts (sums of the
-//                segment counts; 2048 tiles per CTA,
-//                decoupled look-back across CTAs, bounded waits); E.
-//   K3 place     a warp per tile (BF16) or four (E5M2): segment offsets by
-//                shuffle scan, escapes
-//                copied to their final places, chunk offsets at chunk starts.
-//                A segment whose escapes do not all fit in its warp's list is
-//                rebuilt from the input in element order.
+//   dense   one resident wave of CTAs drawing 8192-element tiles from a
+//           counter: input staged through a per-thread cp.async ring, field
+//           split, code lookup in shared-memory word tables, dense code and
+//           sign+mantissa stores.  Each warp ranks the escapes of its
+//           segments (ballots when no group holds two escapes, else one
+//           shuffle scan) and stores the segments' counts and its first 32
+//           escapes, as one list in element order within each segment, in the
+//           workspace; the tile's count goes to the tile's, its block's and
+//           its superblock's counters.
+//   place   a warp per tile (BF16) or four (E5M2): the tile offsets from the
+//           block and superblock counters (no scan pass, no waits), segment
+//           offsets by shuffle scan, escapes copied to their final places,
+//           chunk offsets at chunk starts.  A segment whose escapes do not all
+//           fit in its warp's list is rebuilt from the input by the whole
+//           warp.  The last CTA writes E and the call's status and re-arms
+//           the counters.
 // Segments: BF16 -- the 256 consecutive elements warp w covers with its group
 // k (element order 8k + w, count slot 4w + k); warp w's list holds its four
 // segments' escapes in order k = 0..3.  E5M2 -- the 1024 elements of warp w,
@@ -44,15 +44,17 @@ constexpr int kTileElems = 8192;     // elements per tile (K1 CTA / K3 warp)
 constexpr int kSegsMax = 32;         // segment slots per tile in the workspace
 constexpr int kEntries = 256;        // escape entries per tile in the workspace
 constexpr int kWarpCap = kEntries / kWarps;  // 32: entries of one warp's escape list
-constexpr int kScanTiles = 2048;     // tiles per K2 CTA (8 per thread)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct MultiPtrs {
     uint64_t* states;
-    uint32_t* tile_excl;
+    uint32_t* tile_tot;  // escapes per tile
     uint16_t* seg_cnt;
     uint16_t* seg_ent;
+    uint32_t* blk;       // escapes per block of kBlockTiles tiles
+    uint32_t* sup;       // escapes per superblock of kSuperTiles tiles
+    uint32_t nblocks, nsupers;
 };
 
 // Stores of segment counts and escape list entries: under the L2 policy pol
@@ -258,17 +260,18 @@ struct Bf16Dense {
     // (almost every tile at KV-cache escape rates): a group's rank is the
     // number of lower lanes whose same group has an escape, a segment's total
     // the population of that ballot.
-    static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
-                                                           uint16_t* ent, const uint8_t* in,
-                                                           uint64_t pol) {
+    // Both return the warp's escape count (the same in every lane).
+    static __device__ __forceinline__ uint32_t bookkeep_single(const Keep& kp, uint16_t* row,
+                                                               uint16_t* ent, const uint8_t* in,
+                                                               uint64_t pol) {
         const uint32_t lane = threadIdx.x & 31, lt = (1u << lane) - 1u;
         uint32_t has[kGroups];
 #pragma unroll
         for (int k = 0; k < kGroups; k++) has[k] = __ballot_sync(0xFFFFFFFFu, kp.miss[k] != 0);
         const uint32_t c0 = __popc(has[0]), c1 = __popc(has[1]), c2 = __popc(has[2]);
+        const uint32_t c3 = __popc(has[3]);
         if (lane == 0)
-            st_list8<kKeepLists>(row + slot(0),
-                                 make_uint2(c0 | (c1 << 16), c2 | (__popc(has[3]) << 16)), pol);
+            st_list8<kKeepLists>(row + slot(0), make_uint2(c0 | (c1 << 16), c2 | (c3 << 16)), pol);
         if (kp.cnt) {
             uint32_t excl = 0;
 #pragma unroll
@@ -276,12 +279,13 @@ struct Bf16Dense {
             const uint32_t base[kGroups] = {0u, c0, c0 + c1, c0 + c1 + c2};
             emit(kp, excl, base, ent, in, pol);
         }
+        return c0 + c1 + c2 + c3;
     }
     // Counts and escapes in general: one packed warp scan of the four groups'
     // counts.
-    static __device__ __forceinline__ void bookkeep_multi(const Keep& kp, uint16_t* row,
-                                                          uint16_t* ent, const uint8_t* in,
-                                                          uint64_t pol) {
+    static __device__ __forceinline__ uint32_t bookkeep_multi(const Keep& kp, uint16_t* row,
+                                                              uint16_t* ent, const uint8_t* in,
+                                                              uint64_t pol) {
         uint32_t excl, e31, p31;
         warp_scan_excl(kp.cnt, excl, e31, p31);
         const uint32_t t02 = (e31 & 0x00FF00FFu) + (p31 & 0x00FF00FFu);  // totals of groups 0, 2
@@ -295,6 +299,7 @@ struct Bf16Dense {
             const uint32_t base[kGroups] = {0u, c0, c0 + c1, c0 + c1 + c2};
             emit(kp, excl, base, ent, in, pol);
         }
+        return (t02 & 0xFFFFu) + (t02 >> 16) + (t13 & 0xFFFFu) + (t13 >> 16);
     }
 
     // The warp's first kWarpCap escapes into its list.  excl: the exclusive
@@ -487,22 +492,24 @@ struct E5m2Dense {
 
     static __device__ __forceinline__ bool multi(const Keep& kp) { return kp.cnt >= 2; }
     // Counts and escapes when no lane of the warp holds more than one escape.
-    static __device__ __forceinline__ void bookkeep_single(const Keep& kp, uint16_t* row,
-                                                           uint16_t* ent, const uint8_t* in,
-                                                           uint64_t pol) {
+    static __device__ __forceinline__ uint32_t bookkeep_single(const Keep& kp, uint16_t* row,
+                                                               uint16_t* ent, const uint8_t* in,
+                                                               uint64_t pol) {
         const uint32_t lane = threadIdx.x & 31;
         const uint32_t has = __ballot_sync(0xFFFFFFFFu, kp.cnt != 0);
         if (lane == 0) st_list2<kKeepLists>(row + slot(0), __popc(has), pol);
         if (kp.cnt) emit(kp, __popc(has & ((1u << lane) - 1u)), ent, in, pol);
+        return __popc(has);
     }
 
-    static __device__ __forceinline__ void bookkeep_multi(const Keep& kp, uint16_t* row,
-                                                          uint16_t* ent, const uint8_t* in,
-                                                          uint64_t pol) {
+    static __device__ __forceinline__ uint32_t bookkeep_multi(const Keep& kp, uint16_t* row,
+                                                              uint16_t* ent, const uint8_t* in,
+                                                              uint64_t pol) {
         uint32_t excl, e31, p31;
         warp_scan_excl(kp.cnt, excl, e31, p31);
         if ((threadIdx.x & 31) == 0) st_list2<kKeepLists>(row + slot(0), e31 + p31, pol);
         if (kp.cnt) emit(kp, excl, ent, in, pol);
+        return e31 + p31;
     }
     // One segment per warp: segment s's entries are warp s's whole list.
     static __device__ __forceinline__ uint32_t seg_list(uint32_t s) { return s; }
@@ -556,8 +563,12 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
     extern __shared__ uint4 ring[];  // [S][L][kThreads]
     __shared__ typename F::Tables tables;
     __shared__ uint32_t s_grab[3];   // tile ids drawn by thread 0: [0..1] alternate, [2] the first pair
+    __shared__ uint32_t s_tot[2];    // the tile's escape count, summed over the warps (alternate)
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
-    if (threadIdx.x == 0) s_grab[2] = atomicAdd(&hdr->dense_next, (uint32_t)S);
+    if (threadIdx.x == 0) {
+        s_grab[2] = atomicAdd(&hdr->dense_next, (uint32_t)S);
+        s_tot[0] = s_tot[1] = 0;
+    }
     {
         uint32_t cbw[4];
         codebook_words(a.dcb, a.cbw, cbw);
@@ -598,12 +609,21 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
         // The bookkeeping reads escapes from the stage: refill after it.
         uint16_t* row = p.seg_cnt + (size_t)tile * kSegsMax;
         uint16_t* ent = p.seg_ent + (size_t)tile * kEntries;
-        if (!__any_sync(0xFFFFFFFFu, F::multi(kp))) {
-            F::bookkeep_single(kp, row, ent, in, keep);
-        } else {
-            F::bookkeep_multi(kp, row, ent, in, keep);
+        const uint32_t wt = !__any_sync(0xFFFFFFFFu, F::multi(kp))
+                                ? F::bookkeep_single(kp, row, ent, in, keep)
+                                : F::bookkeep_multi(kp, row, ent, in, keep);
+        if ((threadIdx.x & 31) == 0 && wt) atomicAdd(&s_tot[it & 1], wt);
+        __syncthreads();  // the drawn id and the tile's count are in; every lane has read the stage
+        if (threadIdx.x == 0) {
+            // The tile's escape count, and its block's and superblock's, for placement.
+            const uint32_t tot = s_tot[it & 1];
+            s_tot[it & 1] = 0;  // written again two tiles on, after the next barrier
+            p.tile_tot[tile] = tot;
+            if (tot) {
+                atomicAdd(p.blk + tile / kBlockTiles, tot);
+                atomicAdd(p.sup + tile / kSuperTiles, tot);
+            }
         }
-        __syncthreads();  // the drawn id is visible; every lane has read the stage
         const uint32_t ahead = s_grab[it & 1];
         fill(ahead, slot);
         slot = slot + 1 == S ? 0 : slot + 1;
@@ -614,116 +634,108 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
     if (threadIdx.x == 0 && it) atomicAdd(&hdr->dense_done, it);  // tiles this CTA processed
 }
 
-// -------------------------------------------------------------- K2 prefix
+// ------------------------------------------------------ escape offsets
+//
+// The dense pass adds each tile's escape count to its block's (kBlockTiles
+// tiles) and its superblock's (kSuperTiles tiles) counter.  The exclusive
+// escape offset of tile t is then the sum over the superblocks before t's,
+// the blocks of t's superblock before t's block, and the tiles of t's block
+// before t: a warp finds the offsets of a whole block with one round of
+// loads (at most 4 + 2 + 2 per lane) and warp scans, with no pass of its own
+// and no waits.
 
-// Last CTA of a prefix launch: move the status bits out and re-arm the
-// header.  Each CTA draws exactly one ticket, so a clean launch leaves
-// gridDim.x tickets; anything else means the header did not start zeroed.
-__device__ void prefix_finished(const EncodeArgs& a, uint32_t epoch) {
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
-    __threadfence();
-    const uint32_t prev = atomicAdd(&hdr->done, 1u);
-    if (prev == gridDim.x - 1) {
-        __threadfence();
-        const uint32_t tickets = atomicAdd(&hdr->ticket, 0u);
-        const uint32_t dense_done = atomicAdd(&hdr->dense_done, 0u);
-        const bool timed_out = (atomicAdd(&hdr->status, 0u) & kStatusTimeout) != 0;
-        // Every tile processed exactly once, every prefix CTA drew one ticket.
-        if (!timed_out && (tickets != gridDim.x || dense_done != a.num_tiles))
-            atomicOr(&hdr->status, kStatusBadWorkspace);
-        hdr->last_status = atomicExch(&hdr->status, 0u);
-        hdr->ticket = 0;
-        hdr->done = 0;
-        hdr->dense_next = 0;
-        hdr->dense_done = 0;
-        hdr->epoch = epoch + 1u;
-        __threadfence();
-    }
-}
-
-template <int SEGS, uint32_t kMaxExp>
-__global__ void __launch_bounds__(kThreads) prefix_kernel(const EncodeArgs a, const MultiPtrs p,
-                                                          uint32_t num_tiles, uint32_t num_blocks) {
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
-    __shared__ uint32_t s_blk, s_epoch, s_excl;
-    __shared__ uint32_t s_warp[kWarps];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        s_blk = atomicAdd(&hdr->ticket, 1u);  // blocks in start order: predecessors are running
-        s_epoch = *reinterpret_cast<volatile uint32_t*>(&hdr->epoch);
-    }
-    __syncthreads();
-    const uint32_t blk = s_blk, epoch = s_epoch;
-    if (blk >= num_blocks) {  // the header did not start zeroed: touch nothing else
-        if (tid == 0) {
-            atomicOr(&hdr->status, kStatusBadWorkspace);
-            prefix_finished(a, epoch);
-        }
-        return;
-    }
-    // Tile totals: the sum of each tile's segment counts (16-bit, 32 slots per
-    // tile, the first SEGS in use).  The row count is a constant, so all of a
-    // thread's row loads are issued before the first is summed.
-    const uint32_t base = blk * (uint32_t)kScanTiles + tid * 8;
-    uint32_t v[8];
+// For the block holding tile `first`: before = the escapes of all tiles before
+// the block; ex_lo / ex_hi = the exclusive offset, inside the block, of the
+// block's tile `lane` / `32 + lane`.  All lanes call it.
+__device__ __forceinline__ void block_offsets(const MultiPtrs& p, uint32_t first,
+                                              uint32_t num_tiles, uint32_t& before,
+                                              uint32_t& ex_lo, uint32_t& ex_hi) {
+    static_assert(kBlockTiles == 64 && kSuperTiles % kBlockTiles == 0, "two tiles per lane");
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t sp = first / kSuperTiles, bk = first / kBlockTiles, t0 = bk * kBlockTiles;
+    const uint32_t v_lo = t0 + lane < num_tiles ? __ldcg(p.tile_tot + t0 + lane) : 0u;
+    const uint32_t v_hi = t0 + 32 + lane < num_tiles ? __ldcg(p.tile_tot + t0 + 32 + lane) : 0u;
+    uint32_t acc = 0;
+    for (uint32_t i = lane; i < sp; i += 32) acc += __ldcg(p.sup + i);
+    for (uint32_t i = sp * (kSuperTiles / kBlockTiles) + lane; i < bk; i += 32) acc += __ldcg(p.blk + i);
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-        v[i] = 0;
-        if (base + i >= num_tiles) continue;
-        const uint4* row = reinterpret_cast<const uint4*>(p.seg_cnt + (size_t)(base + i) * kSegsMax);
-        static_assert(SEGS % 8 == 0 && SEGS <= kSegsMax, "whole 16-byte rows of counts");
-#pragma unroll
-        for (int q = 0; q < SEGS / 8; q++) {
-            const uint4 c = row[q];
-            const uint32_t w = (c.x & 0xFFFFu) + (c.x >> 16) + (c.y & 0xFFFFu) + (c.y >> 16) +
-                               (c.z & 0xFFFFu) + (c.z >> 16) + (c.w & 0xFFFFu) + (c.w >> 16);
-            v[i] += w;
-        }
-    }
-    uint32_t sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; i++) sum += v[i];
-    uint32_t incl = sum;
+    for (int d = 16; d; d >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, d);
+    uint32_t lo = v_lo, hi = v_hi;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += u;
+        const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, lo, d), w = __shfl_up_sync(0xFFFFFFFFu, hi, d);
+        if (lane >= (uint32_t)d) {
+            lo += u;
+            hi += w;
+        }
     }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    uint32_t pre = 0, agg = 0;
+    before = acc;
+    ex_lo = lo - v_lo;
+    ex_hi = hi - v_hi + __shfl_sync(0xFFFFFFFFu, lo, 31);
+}
+
+// Offset of the block's tile j (0 <= j < 64) from block_offsets' results; all
+// lanes call it, each with its own j.
+__device__ __forceinline__ uint32_t offset_in_block(uint32_t before, uint32_t ex_lo,
+                                                    uint32_t ex_hi, uint32_t j) {
+    const uint32_t a = __shfl_sync(0xFFFFFFFFu, ex_lo, j & 31u);
+    const uint32_t b = __shfl_sync(0xFFFFFFFFu, ex_hi, j & 31u);
+    return before + (j < 32 ? a : b);
+}
+
+// Run by every thread of the last placement CTA to finish, after all others:
+// E is the sum of the superblock counters; chunk_off[C], the status bits and
+// the checks of the call; the counters are zeroed for the next encode.
+// Every tile processed exactly once and blocks adding up to the superblocks
+// show a workspace that started consistent.
+template <class F>
+__device__ void place_finish(const EncodeArgs& a, const MultiPtrs& p) {
+    __shared__ uint32_t s_part[2][kWarps];
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __threadfence();
+    uint32_t e_sup = 0, e_blk = 0;
+    for (uint32_t i = threadIdx.x; i < p.nsupers; i += kThreads) {
+        e_sup += __ldcg(p.sup + i);
+        p.sup[i] = 0;
+    }
+    for (uint32_t i = threadIdx.x; i < p.nblocks; i += kThreads) {
+        e_blk += __ldcg(p.blk + i);
+        p.blk[i] = 0;
+    }
 #pragma unroll
-    for (int w = 0; w < kWarps; w++) {
-        pre += w < warp ? s_warp[w] : 0u;
-        agg += s_warp[w];
+    for (int d = 16; d; d >>= 1) {
+        e_sup += __shfl_xor_sync(0xFFFFFFFFu, e_sup, d);
+        e_blk += __shfl_xor_sync(0xFFFFFFFFu, e_blk, d);
     }
-    if (warp == 0) {
-        uint64_t* states = p.states;
-        if (lane == 0)
-            publish_count(states, blk, epoch, agg, (a.test_flags & kTestStallFirstTile) != 0);
-        const uint32_t excl = look_back(states, &hdr->status, blk, epoch, agg, a.spin_limit);
-        if (lane == 0) s_excl = excl;
+    if (lane == 0) {
+        s_part[0][warp] = e_sup;
+        s_part[1][warp] = e_blk;
     }
     __syncthreads();
-    uint32_t running = s_excl + pre + incl - sum;
+    if (threadIdx.x == 0) {
+        uint32_t total = 0, blocks = 0;
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-        if (base + i < num_tiles) p.tile_excl[base + i] = running;
-        running += v[i];
-    }
-    if (blk == num_blocks - 1 && tid == 0) {
-        const uint32_t total = s_excl + agg;
+        for (int w = 0; w < kWarps; w++) {
+            total += s_part[0][w];
+            blocks += s_part[1][w];
+        }
         a.chunk_off[a.nchunks] = total;
         hdr->last_escapes = total;
         if ((uint64_t)total > a.esc_capacity) atomicOr(&hdr->status, kStatusOverflow);
         if (a.dcb) {  // a codebook from device memory is checked here, once per encode
             uint32_t cbw[4];
             codebook_words(a.dcb, a.cbw, cbw);
-            if (!codebook_valid(cbw, kMaxExp)) atomicOr(&hdr->status, kStatusBadCodebook);
+            if (!codebook_valid(cbw, F::kExpMask)) atomicOr(&hdr->status, kStatusBadCodebook);
         }
+        if (atomicAdd(&hdr->dense_done, 0u) != a.num_tiles || blocks != total)
+            atomicOr(&hdr->status, kStatusBadWorkspace);
+        hdr->last_status = atomicExch(&hdr->status, 0u);
+        hdr->done = 0;
+        hdr->dense_next = 0;
+        hdr->dense_done = 0;
+        __threadfence();
     }
-    __syncthreads();
-    if (tid == 0) prefix_finished(a, epoch);
 }
 
 // --------------------------------------------------------------- K3 place
@@ -826,10 +838,13 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
     constexpr uint32_t kOffMask = (1u << F::kOffBits) - 1u;
     constexpr uint32_t SEGS = F::kSegs, TPW = 32 / F::kSegs;
     constexpr int K = F::kPreload;
+    static_assert(kBlockTiles % (TPW * R) == 0, "a warp's tiles lie in one block");
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __shared__ uint8_t isesc_all[kWarps][256];  // per warp: 1 for an exponent outside the codebook
+    __shared__ uint32_t s_last;
     uint8_t* isesc = isesc_all[warp];
     const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW * R;
+  auto work = [&]() {  // this warp's tiles; returns early, never leaves the kernel
     if (tile0 >= num_tiles) return;  // warp-uniform
     const uint32_t sub = lane / SEGS, sgl = lane % SEGS;  // this lane's tile and segment
     const uint32_t lbase = lane & ~(SEGS - 1);
@@ -840,9 +855,18 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
 #pragma unroll
     for (int r = 0; r < R; r++) {
         const uint32_t tile = tile_of(r);
-        const bool tv = tile < num_tiles;
-        excl[r] = tv ? p.tile_excl[tile] : 0u;
-        cnt[r] = tv ? ld_last2(p.seg_cnt + (size_t)tile * kSegsMax + F::storage(sgl)) : 0u;
+        cnt[r] = tile < num_tiles ? ld_last2(p.seg_cnt + (size_t)tile * kSegsMax + F::storage(sgl)) : 0u;
+    }
+    {
+        uint32_t before, ex_lo, ex_hi;
+        block_offsets(p, tile0, num_tiles, before, ex_lo, ex_hi);
+        const uint32_t b0 = tile0 / kBlockTiles * kBlockTiles;
+#pragma unroll
+        for (int r = 0; r < R; r++) {
+            const uint32_t tile = tile_of(r);
+            const uint32_t o = offset_in_block(before, ex_lo, ex_hi, tile - b0);
+            excl[r] = tile < num_tiles ? o : 0u;
+        }
     }
 #pragma unroll
     for (int r = 0; r < R; r++) {
@@ -1002,27 +1026,37 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
         }
     }
     release();
+  };
+    work();
+    // The last CTA to finish totals the escapes, checks and re-arms the call.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(&reinterpret_cast<WsHeader*>(a.ws)->done, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) place_finish<F>(a, p);
 }
 
 template <class F>
-cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
+cudaError_t launch_two(const EncodeArgs& a, cudaStream_t s) {
     const MultiLayout L = multi_layout(a.n);
     MultiPtrs p;
     p.states = reinterpret_cast<uint64_t*>(a.ws + L.states);
-    p.tile_excl = reinterpret_cast<uint32_t*>(a.ws + L.tile_excl);
+    p.tile_tot = reinterpret_cast<uint32_t*>(a.ws + L.tile_tot);
     p.seg_cnt = reinterpret_cast<uint16_t*>(a.ws + L.seg_cnt);
     p.seg_ent = reinterpret_cast<uint16_t*>(a.ws + L.seg_ent);
+    p.blk = reinterpret_cast<uint32_t*>(a.ws + L.sums);
+    p.sup = p.blk + (kWsSumsBytes / 4 - ((1ull << 32) / kTileElems) / kSuperTiles);  // fixed place
+    p.nblocks = (uint32_t)L.nblocks;
+    p.nsupers = (uint32_t)L.nsupers;
     const uint32_t tiles = a.num_tiles;
-    const uint32_t blocks = (tiles + kScanTiles - 1) / kScanTiles;
     constexpr size_t smem = dense_smem_bytes<F>();
     Wave wv;
     cudaError_t e = launch_wave<dense_kernel<F>>(kThreads, smem, wv);
     if (e != cudaSuccess) return e;
     const uint64_t wave = wv.ctas();
     dense_kernel<F><<<(uint32_t)(tiles < wave ? tiles : wave), kThreads, smem, s>>>(a, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    prefix_kernel<F::kSegs, F::kExpMask><<<blocks, kThreads, 0, s>>>(a, p, tiles, blocks);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // Placement takes F::kPlaceRounds rounds of tiles per warp, or one round
@@ -1043,22 +1077,25 @@ cudaError_t launch_three(const EncodeArgs& a, cudaStream_t s) {
 MultiLayout multi_layout(uint64_t n) {
     const uint64_t tiles = n ? (n + kTileElems - 1) / kTileElems : 1;
     MultiLayout L;
-    size_t off = kWsHeaderBytes;
+    L.sums = kWsHeaderBytes;  // fixed offset and size, whatever n is
+    size_t off = kWsStatesOffset;
     L.states = off;
     off += align256(8 * tiles);
-    L.tile_excl = off;
+    L.tile_tot = off;
     off += align256(4 * tiles);
     L.seg_cnt = off;
     off += align256(2 * kSegsMax * tiles);
     L.seg_ent = off;
     off += align256(2 * kEntries * tiles);
+    L.nblocks = (tiles + kBlockTiles - 1) / kBlockTiles;
+    L.nsupers = (tiles + kSuperTiles - 1) / kSuperTiles;
     L.bytes = off;
     return L;
 }
 
 cudaError_t launch_encode_multi(const EncodeArgs& a, bool e5m2, cudaStream_t s) {
     if (a.num_tiles == 0) return cudaSuccess;
-    return e5m2 ? launch_three<E5m2Dense>(a, s) : launch_three<Bf16Dense>(a, s);
+    return e5m2 ? launch_two<E5m2Dense>(a, s) : launch_two<Bf16Dense>(a, s);
 }
 
 }  // namespace splitzip

@@ -27,7 +27,7 @@ namespace {
 
 constexpr uint64_t kNoAllocMaxElements = SPLITZIP_NOALLOC_MAX_ELEMENTS;
 constexpr uint64_t kNoAllocTiles = kNoAllocMaxElements / 8192;  // BF16 encode tile
-constexpr size_t kNoAllocScratchBytes = kWsHeaderBytes + 8 * kNoAllocTiles;
+constexpr size_t kNoAllocScratchBytes = kWsStatesOffset + 8 * kNoAllocTiles;
 
 // Every GPU that loads the library holds this array (about 2 MiB) until exit.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];

@@ -64,22 +64,26 @@ struct CalibArgs {
 // start (256-byte aligned):
 //   [0, 4096)            header (WsHeader)
 //   states               8 bytes per tile: look-back state words (the single-
-//                        launch pipeline uses one per tile, the tile-prefix
-//                        kernel one per 2048 tiles)
-//   tile_excl            4 bytes per tile: exclusive prefix of the tiles'
-//                        escape counts
+//                        launch pipeline)
+//   tile_tot             4 bytes per tile: the tile's escape count
 //   seg_cnt              32 x uint16 per tile: escapes per segment
 //   seg_ent              256 x uint16 per tile: per warp, a list of its first
 //                        32 escapes (position in segment | exponent << offset bits)
+//   sums                 (right after the header, fixed size) uint32 escape
+//                        counts of blocks of kBlockTiles tiles, then of
+//                        superblocks of kSuperTiles tiles (zero between encodes)
+constexpr uint32_t kBlockTiles = 64;
+constexpr uint32_t kSuperTiles = 4096;
 struct MultiLayout {
-    size_t states, tile_excl, seg_cnt, seg_ent, bytes;
+    size_t states, tile_tot, seg_cnt, seg_ent, sums, bytes;
+    uint64_t nblocks, nsupers;
 };
 MultiLayout multi_layout(uint64_t n);
 
 int encode_tile_elems(bool e5m2);
 int decode_tile_elems(bool e5m2);
 cudaError_t launch_encode(const EncodeArgs& a, bool e5m2, cudaStream_t s);        // one launch
-cudaError_t launch_encode_multi(const EncodeArgs& a, bool e5m2, cudaStream_t s);  // three launches
+cudaError_t launch_encode_multi(const EncodeArgs& a, bool e5m2, cudaStream_t s);  // two launches
 cudaError_t launch_decode(const DecodeArgs& a, bool e5m2, cudaStream_t s);
 cudaError_t launch_calibrate(const CalibArgs& a, bool e5m2, cudaStream_t s);
 uint32_t calibrate_grid(uint32_t n, int num_sms);

@@ -66,16 +66,19 @@ def test_stream_sizes(lib):
         assert sz.splitzip_signman_bytes(n, "bf16") == n
         assert sz.splitzip_signman_bytes(n, "e5m2") == (3 * n + 7) // 8
         assert sz.splitzip_num_chunks(n, 1024) == -(-n // 1024)
-    # 4 KiB header, then per 8192-element tile: an 8-byte look-back word, a
-    # 4-byte prefix, 32 uint16 segment counts and 256 uint16 escape entries,
-    # each array rounded up to 256 bytes.
+    # 4 KiB header, a uint32 escape count per block of 64 tiles and per
+    # superblock of 4096 tiles for the largest element count (fixed size),
+    # then per 8192-element tile: an 8-byte look-back word, a 4-byte escape
+    # count, 32 uint16 segment counts and 256 uint16 escape entries; each
+    # array rounded up to 256 bytes.
+    sums = 4 * (2**19 // 64 + 2**19 // 4096)
     def expect(n):
         t = -(-n // 8192)
         a = lambda v: -(-v // 256) * 256
-        return 4096 + a(8 * t) + a(4 * t) + a(64 * t) + a(512 * t)
+        return 4096 + sums + a(8 * t) + a(4 * t) + a(64 * t) + a(512 * t)
     for n in (1, 8192, 8193, 10**6, 2**31, 2**32 - 1):
         assert sz.splitzip_workspace_bytes(n) == expect(n)
-    assert sz.splitzip_workspace_bytes(2**31) == 4096 + 588 * 2**18
+    assert sz.splitzip_workspace_bytes(2**31) == 4096 + 33280 + 588 * 2**18
 
 
 def test_chunk_division_multiplier():

@@ -79,13 +79,14 @@ def test_escape_overflow(fmt):
     assert_streams_equal(again, ref, "after overflow")
 
 
-@pytest.mark.parametrize("engine", ["multi", "pipelined"])
 @pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
-def test_lookback_wait_gives_up(fmt, engine):
-    """The first tile (pipelined) or first block of 2048 tiles (three-launch
-    encode) never publishes its prefix; its successor polls 2000 times,
-    records TIMEOUT and returns.  The context stays usable."""
-    n = 40_000 if engine == "pipelined" else 2048 * 8192 + 100
+def test_lookback_wait_gives_up(fmt):
+    """The single-launch pipeline's first tile never publishes its prefix;
+    its successor polls 2000 times, records TIMEOUT and returns.  The context
+    stays usable and the next call on the workspace is correct.  (The default
+    two-launch encode has no waits to run out.)"""
+    engine = "pipelined"
+    n = 40_000
     x, cb = _setup(n=n, fmt=fmt)
     ws = sz.alloc_workspace(n, DEV)
     st = sz.alloc_streams(n, 1024, fmt, esc_capacity=n)
