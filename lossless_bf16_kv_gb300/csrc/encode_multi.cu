@@ -52,7 +52,7 @@ struct MultiPtrs {
     uint32_t* tile_tot;  // escapes per tile
     uint16_t* seg_cnt;
     uint16_t* seg_ent;
-    uint32_t* blk;       // escapes per block of kBlockTiles tiles
+    uint32_t* blk;       // per block of kBlockTiles tiles: escapes | tiles done << kBlkCountShift
     uint32_t* sup;       // escapes per superblock of kSuperTiles tiles
     uint32_t nblocks, nsupers;
 };
@@ -615,13 +615,19 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
         if ((threadIdx.x & 31) == 0 && wt) atomicAdd(&s_tot[it & 1], wt);
         __syncthreads();  // the drawn id and the tile's count are in; every lane has read the stage
         if (threadIdx.x == 0) {
-            // The tile's escape count, and its block's and superblock's, for placement.
+            // The tile's escape count, and its block's, for placement.  The
+            // tile that completes its block adds the block's count to the
+            // superblock's: tiles in flight lie in a window of consecutive
+            // tiles, so a per-tile add there would make one hot address.
             const uint32_t tot = s_tot[it & 1];
             s_tot[it & 1] = 0;  // written again two tiles on, after the next barrier
             p.tile_tot[tile] = tot;
-            if (tot) {
-                atomicAdd(p.blk + tile / kBlockTiles, tot);
-                atomicAdd(p.sup + tile / kSuperTiles, tot);
+            const uint32_t bk = tile / kBlockTiles, left = a.num_tiles - bk * kBlockTiles;
+            const uint32_t in_block = left < kBlockTiles ? left : kBlockTiles;
+            const uint32_t old = atomicAdd(p.blk + bk, tot + (1u << kBlkCountShift));
+            if ((old >> kBlkCountShift) == in_block - 1u) {
+                const uint32_t btot = (old & kBlkEscMask) + tot;
+                if (btot) atomicAdd(p.sup + tile / kSuperTiles, btot);
             }
         }
         const uint32_t ahead = s_grab[it & 1];
@@ -637,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
 // ------------------------------------------------------ escape offsets
 //
 // The dense pass adds each tile's escape count to its block's (kBlockTiles
-// tiles) and its superblock's (kSuperTiles tiles) counter.  The exclusive
+// tiles) counter, and each block's to its superblock's (kSuperTiles tiles).  The exclusive
 // escape offset of tile t is then the sum over the superblocks before t's,
 // the blocks of t's superblock before t's block, and the tiles of t's block
 // before t: a warp finds the offsets of a whole block with one round of
@@ -657,7 +663,8 @@ __device__ __forceinline__ void block_offsets(const MultiPtrs& p, uint32_t first
     const uint32_t v_hi = t0 + 32 + lane < num_tiles ? __ldcg(p.tile_tot + t0 + 32 + lane) : 0u;
     uint32_t acc = 0;
     for (uint32_t i = lane; i < sp; i += 32) acc += __ldcg(p.sup + i);
-    for (uint32_t i = sp * (kSuperTiles / kBlockTiles) + lane; i < bk; i += 32) acc += __ldcg(p.blk + i);
+    for (uint32_t i = sp * (kSuperTiles / kBlockTiles) + lane; i < bk; i += 32)
+        acc += __ldcg(p.blk + i) & kBlkEscMask;
 #pragma unroll
     for (int d = 16; d; d >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, d);
     uint32_t lo = v_lo, hi = v_hi;
@@ -690,35 +697,40 @@ __device__ __forceinline__ uint32_t offset_in_block(uint32_t before, uint32_t ex
 // show a workspace that started consistent.
 template <class F>
 __device__ void place_finish(const EncodeArgs& a, const MultiPtrs& p) {
-    __shared__ uint32_t s_part[2][kWarps];
+    __shared__ uint32_t s_part[3][kWarps];
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __threadfence();
-    uint32_t e_sup = 0, e_blk = 0;
+    uint32_t e_sup = 0, e_blk = 0, t_blk = 0;
     for (uint32_t i = threadIdx.x; i < p.nsupers; i += kThreads) {
         e_sup += __ldcg(p.sup + i);
         p.sup[i] = 0;
     }
     for (uint32_t i = threadIdx.x; i < p.nblocks; i += kThreads) {
-        e_blk += __ldcg(p.blk + i);
+        const uint32_t v = __ldcg(p.blk + i);
+        e_blk += v & kBlkEscMask;
+        t_blk += v >> kBlkCountShift;
         p.blk[i] = 0;
     }
 #pragma unroll
     for (int d = 16; d; d >>= 1) {
         e_sup += __shfl_xor_sync(0xFFFFFFFFu, e_sup, d);
         e_blk += __shfl_xor_sync(0xFFFFFFFFu, e_blk, d);
+        t_blk += __shfl_xor_sync(0xFFFFFFFFu, t_blk, d);
     }
     if (lane == 0) {
         s_part[0][warp] = e_sup;
         s_part[1][warp] = e_blk;
+        s_part[2][warp] = t_blk;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t total = 0, blocks = 0;
+        uint32_t total = 0, blocks = 0, counted = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; w++) {
             total += s_part[0][w];
             blocks += s_part[1][w];
+            counted += s_part[2][w];
         }
         a.chunk_off[a.nchunks] = total;
         hdr->last_escapes = total;
@@ -728,7 +740,8 @@ __device__ void place_finish(const EncodeArgs& a, const MultiPtrs& p) {
             codebook_words(a.dcb, a.cbw, cbw);
             if (!codebook_valid(cbw, F::kExpMask)) atomicOr(&hdr->status, kStatusBadCodebook);
         }
-        if (atomicAdd(&hdr->dense_done, 0u) != a.num_tiles || blocks != total)
+        if (atomicAdd(&hdr->dense_done, 0u) != a.num_tiles || counted != a.num_tiles ||
+            blocks != total)
             atomicOr(&hdr->status, kStatusBadWorkspace);
         hdr->last_status = atomicExch(&hdr->status, 0u);
         hdr->done = 0;

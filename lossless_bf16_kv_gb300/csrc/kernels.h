@@ -69,11 +69,15 @@ struct CalibArgs {
 //   seg_cnt              32 x uint16 per tile: escapes per segment
 //   seg_ent              256 x uint16 per tile: per warp, a list of its first
 //                        32 escapes (position in segment | exponent << offset bits)
-//   sums                 (right after the header, fixed size) uint32 escape
-//                        counts of blocks of kBlockTiles tiles, then of
-//                        superblocks of kSuperTiles tiles (zero between encodes)
+//   sums                 (right after the header, fixed size) uint32 words of
+//                        blocks of kBlockTiles tiles (escape count in the low
+//                        kBlkCountShift bits, tiles counted above them), then
+//                        escape counts of superblocks of kSuperTiles tiles
+//                        (zero between encodes)
 constexpr uint32_t kBlockTiles = 64;
 constexpr uint32_t kSuperTiles = 4096;
+constexpr uint32_t kBlkCountShift = 24;  // a block holds at most 64 x 8192 = 2^19 escapes
+constexpr uint32_t kBlkEscMask = (1u << kBlkCountShift) - 1u;
 struct MultiLayout {
     size_t states, tile_tot, seg_cnt, seg_ent, sums, bytes;
     uint64_t nblocks, nsupers;
