@@ -44,6 +44,9 @@ constexpr int kTileElems = 8192;     // elements per tile (K1 CTA / K3 warp)
 constexpr int kSegsMax = 32;         // segment slots per tile in the workspace
 constexpr int kEntries = 256;        // escape entries per tile in the workspace
 constexpr int kWarpCap = kEntries / kWarps;  // 32: entries of one warp's escape list
+// Superblocks of the largest tensor (2^32 - 1 elements).
+constexpr uint32_t kMaxSupers = (uint32_t)(((1ull << 32) / kTileElems) / kSuperTiles);  // 128
+static_assert(kMaxSupers % 32 == 0, "whole superblock counts per lane");
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -656,15 +659,31 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
 __device__ __forceinline__ void block_offsets(const MultiPtrs& p, uint32_t first,
                                               uint32_t num_tiles, uint32_t& before,
                                               uint32_t& ex_lo, uint32_t& ex_hi) {
-    static_assert(kBlockTiles == 64 && kSuperTiles % kBlockTiles == 0, "two tiles per lane");
+    static_assert(kBlockTiles == 64 && kSuperTiles % (32 * kBlockTiles) == 0, "two tiles per lane");
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t sp = first / kSuperTiles, bk = first / kBlockTiles, t0 = bk * kBlockTiles;
+    // Every load is issued before any is used (one memory round trip): at
+    // most kMaxSupers / 32 superblock and kSuperTiles / kBlockTiles / 32 block
+    // counts per lane.
+    constexpr uint32_t kSupPerLane = kMaxSupers / 32, kBlkPerLane = kSuperTiles / kBlockTiles / 32;
     const uint32_t v_lo = t0 + lane < num_tiles ? __ldcg(p.tile_tot + t0 + lane) : 0u;
     const uint32_t v_hi = t0 + 32 + lane < num_tiles ? __ldcg(p.tile_tot + t0 + 32 + lane) : 0u;
+    uint32_t vs[kSupPerLane], vb[kBlkPerLane];
+#pragma unroll
+    for (uint32_t k = 0; k < kSupPerLane; k++) {
+        const uint32_t i = lane + 32 * k;
+        vs[k] = i < sp ? __ldcg(p.sup + i) : 0u;
+    }
+#pragma unroll
+    for (uint32_t k = 0; k < kBlkPerLane; k++) {
+        const uint32_t i = sp * (kSuperTiles / kBlockTiles) + lane + 32 * k;
+        vb[k] = i < bk ? __ldcg(p.blk + i) & kBlkEscMask : 0u;
+    }
     uint32_t acc = 0;
-    for (uint32_t i = lane; i < sp; i += 32) acc += __ldcg(p.sup + i);
-    for (uint32_t i = sp * (kSuperTiles / kBlockTiles) + lane; i < bk; i += 32)
-        acc += __ldcg(p.blk + i) & kBlkEscMask;
+#pragma unroll
+    for (uint32_t k = 0; k < kSupPerLane; k++) acc += vs[k];
+#pragma unroll
+    for (uint32_t k = 0; k < kBlkPerLane; k++) acc += vb[k];
 #pragma unroll
     for (int d = 16; d; d >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, d);
     uint32_t lo = v_lo, hi = v_hi;
@@ -1060,7 +1079,7 @@ cudaError_t launch_two(const EncodeArgs& a, cudaStream_t s) {
     p.seg_cnt = reinterpret_cast<uint16_t*>(a.ws + L.seg_cnt);
     p.seg_ent = reinterpret_cast<uint16_t*>(a.ws + L.seg_ent);
     p.blk = reinterpret_cast<uint32_t*>(a.ws + L.sums);
-    p.sup = p.blk + (kWsSumsBytes / 4 - ((1ull << 32) / kTileElems) / kSuperTiles);  // fixed place
+    p.sup = p.blk + (kWsSumsBytes / 4 - kMaxSupers);  // fixed place
     p.nblocks = (uint32_t)L.nblocks;
     p.nsupers = (uint32_t)L.nsupers;
     const uint32_t tiles = a.num_tiles;

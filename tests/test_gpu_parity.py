@@ -98,6 +98,27 @@ def test_multi_tile_ragged(fmt):
         check_roundtrip(x, chunk, cb, f"{fmt} ragged chunk {chunk}")
 
 
+@pytest.mark.parametrize("fmt,layers,tokens,n", [
+    # 4163 full tiles and a ragged one: two superblocks of 4096 tiles, the
+    # last block 4 tiles long; placement in one round of tiles per warp.
+    ("bf16", 1, 16700, 4163 * 8192 + 777),
+    ("e5m2", 1, 16700, 4163 * 8192 + 777),
+    # Tens of thousands of tiles ending 38 tiles into a superblock: placement
+    # in several rounds of tiles per warp (the grid the 2^31-element encode
+    # uses), with a partial last block, superblock and tile.
+    ("bf16", 16, 16400, (1 << 29) + 37 * 8192 + 555),
+    ("e5m2", 20, 16400, 5 * (1 << 27) + 37 * 8192 + 555),
+])
+def test_block_and_superblock_boundaries(fmt, layers, tokens, n):
+    """Escape offsets come from per-tile, per-block (64 tiles) and
+    per-superblock (4096 tiles) counts; sizes that end inside a tile, a block
+    and a superblock must still give the oracle's streams."""
+    dt = torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2
+    x = synth.kv_cache(layers, tokens, seed=9, device=DEV, dtype=dt).reshape(-1)[:n].clone()
+    cb, _ = gpu_calibrate(synth.kv_cache(1, 64, seed=1, device=DEV, dtype=dt))
+    assert check_roundtrip(x, 1024, cb, f"{fmt} n={n}") > 0
+
+
 def test_zero_and_all_escape_tensors():
     cb = list(range(100, 116))
     zeros = torch.zeros(50000, dtype=torch.bfloat16, device=DEV)  # exponent 0: all escapes
