@@ -159,7 +159,7 @@ splitzip_status splitzip_histogram_e5m2(const void* d_x, uint64_t n, uint64_t* d
 
 /* Encode n elements at d_x (16-byte aligned; BF16 or E5M2 bit patterns) with
  * codebook *cb (host memory, copied into the launch) into out's streams
- * (README section Abstract; arXiv abstract).  Two kernel launches, enqueued
+ * (README section Abstract; arXiv abstract).  Three kernel launches, enqueued
  * on s; returns without synchronising.  chunk_size: a multiple of 8 in
  * [8, SPLITZIP_MAX_CHUNK].  1 <= n <= SPLITZIP_MAX_ELEMENTS.
  * If E > esc_capacity, the dense streams and chunk_off are still complete and

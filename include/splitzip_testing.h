@@ -11,7 +11,7 @@
  * bounds and returns, leaving the CUDA context usable.  This entry point lets
  * a test make that wait run out on purpose, with a flag that keeps tile 0
  * from ever publishing, and a small poll limit so the test ends quickly.  (The
- * default two-launch encode has no waits: its tile offsets come from counters
+ * default three-launch encode has no waits: its tile offsets come from counters
  * the first launch completes before the second starts; the stall flag has no
  * effect on it.)  The method's pages have no counterpart: this entry point
  * exists only to exercise the error path.
@@ -29,7 +29,7 @@ extern "C" {
  * (single-launch pipeline only). */
 #define SPLITZIP_TEST_STALL_FIRST_TILE 0x1u
 /* Encode with the single-launch pipeline (the engine of
- * splitzip_encode_noalloc) instead of the two-launch encode. */
+ * splitzip_encode_noalloc) instead of the three-launch encode. */
 #define SPLITZIP_TEST_PIPELINED 0x2u
 
 typedef struct splitzip_encode_test_opts {

@@ -1,4 +1,4 @@
-// encode_multi.cu -- SplitZip encode in two launches (BF16 and FP8 E5M2).
+// encode_multi.cu -- SplitZip encode in three launches (BF16 and FP8 E5M2).
 //
 // Method ("SplitZip: Ultra-Fast Lossless KV Compression for Disaggregated LLM
 // Serving", README section Abstract; arXiv abstract on the paper index page):
@@ -23,7 +23,8 @@
 //           offsets by shuffle scan, escapes copied to their final places,
 //           chunk offsets at chunk starts.  A segment whose escapes do not all
 //           fit in its warp's list is rebuilt from the input by the whole
-//           warp.  The last CTA writes E and the call's status and re-arms
+//           warp.
+//   finish  one CTA: E, chunk_off[C], the call's status and checks; re-arms
 //           the counters.
 // Segments: BF16 -- the 256 consecutive elements warp w covers with its group
 // k (element order 8k + w, count slot 4w + k); warp w's list holds its four
@@ -709,17 +710,17 @@ __device__ __forceinline__ uint32_t offset_in_block(uint32_t before, uint32_t ex
     return before + (j < 32 ? a : b);
 }
 
-// Run by every thread of the last placement CTA to finish, after all others:
-// E is the sum of the superblock counters; chunk_off[C], the status bits and
-// the checks of the call; the counters are zeroed for the next encode.
-// Every tile processed exactly once and blocks adding up to the superblocks
-// show a workspace that started consistent.
+// One CTA after placement: E is the sum of the superblock counters;
+// chunk_off[C], the status bits and the checks of the call; the counters are
+// zeroed for the next encode.  Every tile processed exactly once and blocks
+// adding up to the superblocks show a workspace that started consistent.  (A
+// launch of its own: electing the last placement CTA cost every CTA a fence
+// and a returning atomic while it held its SM slot.)
 template <class F>
-__device__ void place_finish(const EncodeArgs& a, const MultiPtrs& p) {
+__global__ void __launch_bounds__(kThreads) finish_kernel(const EncodeArgs a, const MultiPtrs p) {
     __shared__ uint32_t s_part[3][kWarps];
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    __threadfence();
     uint32_t e_sup = 0, e_blk = 0, t_blk = 0;
     for (uint32_t i = threadIdx.x; i < p.nsupers; i += kThreads) {
         e_sup += __ldcg(p.sup + i);
@@ -873,10 +874,8 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
     static_assert(kBlockTiles % (TPW * R) == 0, "a warp's tiles lie in one block");
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __shared__ uint8_t isesc_all[kWarps][256];  // per warp: 1 for an exponent outside the codebook
-    __shared__ uint32_t s_last;
     uint8_t* isesc = isesc_all[warp];
     const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW * R;
-  auto work = [&]() {  // this warp's tiles; returns early, never leaves the kernel
     if (tile0 >= num_tiles) return;  // warp-uniform
     const uint32_t sub = lane / SEGS, sgl = lane % SEGS;  // this lane's tile and segment
     const uint32_t lbase = lane & ~(SEGS - 1);
@@ -1058,20 +1057,10 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
         }
     }
     release();
-  };
-    work();
-    // The last CTA to finish totals the escapes, checks and re-arms the call.
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        s_last = atomicAdd(&reinterpret_cast<WsHeader*>(a.ws)->done, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (s_last) place_finish<F>(a, p);
 }
 
 template <class F>
-cudaError_t launch_two(const EncodeArgs& a, cudaStream_t s) {
+cudaError_t launch_passes(const EncodeArgs& a, cudaStream_t s) {
     const MultiLayout L = multi_layout(a.n);
     MultiPtrs p;
     p.states = reinterpret_cast<uint64_t*>(a.ws + L.states);
@@ -1101,6 +1090,9 @@ cudaError_t launch_two(const EncodeArgs& a, cudaStream_t s) {
         place_kernel<F, F::kPlaceRounds><<<(tiles + wide - 1) / wide, kThreads, 0, s>>>(a, p, tiles);
     else
         place_kernel<F, 1><<<(tiles + kTilesPerRound - 1) / kTilesPerRound, kThreads, 0, s>>>(a, p, tiles);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    finish_kernel<F><<<1, kThreads, 0, s>>>(a, p);
     return cudaGetLastError();
 }
 
@@ -1127,7 +1119,7 @@ MultiLayout multi_layout(uint64_t n) {
 
 cudaError_t launch_encode_multi(const EncodeArgs& a, bool e5m2, cudaStream_t s) {
     if (a.num_tiles == 0) return cudaSuccess;
-    return e5m2 ? launch_two<E5m2Dense>(a, s) : launch_two<Bf16Dense>(a, s);
+    return e5m2 ? launch_passes<E5m2Dense>(a, s) : launch_passes<Bf16Dense>(a, s);
 }
 
 }  // namespace splitzip

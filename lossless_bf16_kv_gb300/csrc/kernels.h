@@ -87,7 +87,7 @@ MultiLayout multi_layout(uint64_t n);
 int encode_tile_elems(bool e5m2);
 int decode_tile_elems(bool e5m2);
 cudaError_t launch_encode(const EncodeArgs& a, bool e5m2, cudaStream_t s);        // one launch
-cudaError_t launch_encode_multi(const EncodeArgs& a, bool e5m2, cudaStream_t s);  // two launches
+cudaError_t launch_encode_multi(const EncodeArgs& a, bool e5m2, cudaStream_t s);  // three launches
 cudaError_t launch_decode(const DecodeArgs& a, bool e5m2, cudaStream_t s);
 cudaError_t launch_calibrate(const CalibArgs& a, bool e5m2, cudaStream_t s);
 uint32_t calibrate_grid(uint32_t n, int num_sms);

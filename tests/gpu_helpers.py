@@ -40,7 +40,7 @@ def gpu_calibrate(x: torch.Tensor):
 def gpu_encode(x: torch.Tensor, chunk: int, cb, esc_capacity=None, ws=None, engine="multi"):
     """Encode on the GPU; returns (host streams dict, status, E, device streams).
 
-    engine "multi" is splitzip_encode (two launches); "pipelined" is the
+    engine "multi" is splitzip_encode (three launches); "pipelined" is the
     single-launch pipeline behind splitzip_encode_noalloc, reached through the
     test entry point."""
     ensure_library()

@@ -84,7 +84,7 @@ def test_lookback_wait_gives_up(fmt):
     """The single-launch pipeline's first tile never publishes its prefix;
     its successor polls 2000 times, records TIMEOUT and returns.  The context
     stays usable and the next call on the workspace is correct.  (The default
-    two-launch encode has no waits to run out.)"""
+    three-launch encode has no waits to run out.)"""
     engine = "pipelined"
     n = 40_000
     x, cb = _setup(n=n, fmt=fmt)
