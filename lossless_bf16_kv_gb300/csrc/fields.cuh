@@ -47,12 +47,13 @@ __device__ __forceinline__ void split_bf16(uint32_t a, uint32_t b, uint32_t& sm,
 }
 
 // The four three-bit fields (sign << 2 | mantissa) of 4 E5M2 bytes packed in
-// 12 bits, field of byte k at bits 3k..3k+2: with field k in byte k, a byte
-// dot product with (1, 8, 64, 0) places fields 0..2 and field 3 is added on
-// shifted by 9 (fields are below 8, so no sum carries into the next field).
+// 12 bits, field of byte k at bits 3k..3k+2.  With field k in byte k of f,
+// f >> 15 = 512 f3 + 2 f2 (f0 and f1 shift out), and a byte dot product with
+// (1, 8, 62, 0) added to it gives f0 + 8 f1 + 64 f2 + 512 f3 (fields are below
+// 8, so no sum carries into the next field).
 __device__ __forceinline__ uint32_t fields12_e5m2(uint32_t w) {
     const uint32_t f = ((w >> 5) & 0x04040404u) | (w & 0x03030303u);  // field k in byte k
-    return __dp4a(f, 0x00400801u, (f >> 15) & 0xE00u);
+    return __dp4a(f, 0x003E0801u, f >> 15);
 }
 
 // 4 E5M2 bytes -> 4 exponent bytes and the 12 bits of their fields.
