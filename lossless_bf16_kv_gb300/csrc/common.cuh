@@ -269,11 +269,6 @@ __device__ __forceinline__ void st_policy8(void* p, uint2 v, uint64_t pol) {
                  "r"(v.y), "l"(pol)
                  : "memory");
 }
-// Drops the 128-byte L2 line at p (128-byte aligned) without writing it back:
-// its contents become undefined.  For scratch lines no one reads again.
-__device__ __forceinline__ void discard_l2_line(void* p) {
-    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
 // Loads of data read for the last time (evict-first in L2).
 __device__ __forceinline__ uint16_t ld_last2(const void* p) {
     uint16_t v;

@@ -981,24 +981,6 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
         }
     }
 
-    // The warp's count rows and escape lists are dead once it has read them for
-    // the last time: their L2 lines (kept there by the dense pass's evict-last
-    // stores) are dropped without a write-back.  Only whole 128-byte lines
-    // inside this warp's own tiles' rows and lists are dropped.
-    auto release = [&]() {
-        __syncwarp();  // every lane's last read of the rows and lists is done
-        auto drop = [&](const uint16_t* region, uint32_t bytes_per_tile) {
-            const uint32_t t1 = min(tile0 + TPW * (uint32_t)R, num_tiles);
-            const uint64_t b0 = (uint64_t)tile0 * bytes_per_tile, b1 = (uint64_t)t1 * bytes_per_tile;
-            const char* base = reinterpret_cast<const char*>(region);
-            for (uint64_t b = b0 + 128u * lane; b + 128u <= b1; b += 32u * 128u) {
-                char* line = const_cast<char*>(base) + b;
-                if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0) discard_l2_line(line);
-            }
-        };
-        drop(p.seg_cnt, 2 * kSegsMax);
-        drop(p.seg_ent, 2 * kEntries);
-    };
 
     // chunk_off at every chunk start of each of the warp's tiles: the exclusive
     // escape rank of the chunk's first element.  When the chunk size is a
@@ -1016,7 +998,6 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
             const uint32_t qx = chunk_quot(a.cdiv, x);  // x < d + kTileElems
             if (s0 < len && x == qx * a.cdiv.d) a.chunk_off[q0 + qx] = excl[r] + off[r];
         }
-        release();
         return;
     }
 #pragma unroll
@@ -1056,7 +1037,6 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
             }
         }
     }
-    release();
 }
 
 template <class F>

@@ -87,14 +87,15 @@ def test_small_shapes(fmt, chunk):
 @pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
 def test_multi_tile_ragged(fmt):
     # Several encode/decode tiles plus a ragged tail, chunk sizes that do and
-    # do not divide the tile.  256, 512, 2048 and 12288 are multiples of the
-    # BF16 encode segment (256 elements), 2048 and 12288 of the E5M2 one
-    # (1024), and 12288 spans tiles (8192): chunk offsets come from the
-    # segment-start path there and from the general path otherwise.
+    # do not divide the tile.  256 ... 16384 are multiples of the BF16 encode
+    # segment (256 elements), 1024 ... 16384 of the E5M2 one (1024): chunk
+    # offsets come from the segment-start path there (by masks and shifts for
+    # the ones that divide the 8192-element tile; 12288 and 16384 span tiles)
+    # and from the general path otherwise.
     dt = torch.bfloat16 if fmt == "bf16" else torch.float8_e5m2
     x = synth.kv_cache(1, 777, seed=3, device=DEV, dtype=dt).reshape(-1)[:1_500_007]
     cb, _ = gpu_calibrate(synth.kv_cache(1, 64, seed=1, device=DEV, dtype=dt))
-    for chunk in (8, 40, 256, 512, 1000, 1024, 2048, 3000, 12288, 65536):
+    for chunk in (8, 40, 256, 512, 1000, 1024, 2048, 3000, 4096, 8192, 12288, 16384, 65536):
         check_roundtrip(x, chunk, cb, f"{fmt} ragged chunk {chunk}")
 
 
