@@ -20,6 +20,10 @@ constexpr int kWarps = kThreads / 32;
 // [0, 4096)      header (below)
 // then           the encode's block and superblock escape counters (fixed size)
 // then           one 64-bit tile-state word per encode tile
+// The dense pass hands its tiles out from up to kDenseStripes counters: with
+// S stripes, stripe s holds tiles s, s + S, s + 2 S, ...
+constexpr uint32_t kDenseStripes = 4;
+
 struct WsHeader {
     uint32_t ticket;        // encode: next tile id handed to a starting CTA
     uint32_t done;          // encode: CTAs finished in the running launch
@@ -30,10 +34,14 @@ struct WsHeader {
     uint64_t last_escapes;  // encode: E of the last finished launch
     uint64_t cal_covered;   // calibrate: covered count (synchronous API readback)
     uint8_t cal_cb[16];     // calibrate: codebook (synchronous API readback)
-    uint32_t dense_next;    // encode: next tile handed to a CTA of the dense pass
+    uint32_t dense_next;    // encode: the dense pass's tile counter (one stripe)
     uint32_t dense_done;    // encode: tiles the dense pass has processed
     uint64_t reserved[23];
     unsigned long long hist[256];  // calibrate: global exponent histogram, zero between launches
+    // encode: the dense pass's tile counters when it uses several stripes of
+    // tiles, each in a 128-byte line of its own (element [s][0]); zero
+    // between launches.
+    alignas(128) uint32_t dense_stripe[kDenseStripes][32];
 };
 static_assert(sizeof(WsHeader) <= 4096, "header must fit its slot");
 constexpr size_t kWsHeaderBytes = 4096;

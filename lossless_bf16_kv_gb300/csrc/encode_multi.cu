@@ -59,6 +59,7 @@ struct MultiPtrs {
     uint32_t* blk;       // per block of kBlockTiles tiles: escapes | tiles done << kBlkCountShift
     uint32_t* sup;       // escapes per superblock of kSuperTiles tiles
     uint32_t nblocks, nsupers;
+    bool striped;  // the dense pass draws its tiles from F::kStripes counters
 };
 
 // Stores of segment counts and escape list entries: under the L2 policy pol
@@ -123,6 +124,9 @@ struct Bf16Dense {
     // Counts and lists stored plainly: evict-last stores measured 3% slower here.
     static constexpr bool kKeepLists = false;
     static constexpr uint32_t kExpMask = 0xFFu;
+    // Four tile counters, each hit by a quarter of the CTAs' draws (one
+    // counter: 1.164 against 1.158 ms at 2^31 elements).
+    static constexpr uint32_t kStripes = 4;
     struct Tables {
         uint32_t t[4][256];
     };
@@ -374,6 +378,9 @@ struct E5m2Dense {
     };
     static constexpr int kElemBytes = 1;
     static constexpr int kMinBlocks = 6;  // resident CTAs per SM (registers cap it at 40 each)
+    // One tile counter: the whole GPU then works on one window of consecutive
+    // tiles (four stripes: 0.719 -> 0.736 ms at 2^31 elements).
+    static constexpr uint32_t kStripes = 1;
     struct Keep {
         uint32_t mm;   // escape flags of the lane's 32 elements, bit j for element j
         uint32_t cnt;  // popcount of mm
@@ -542,17 +549,21 @@ struct E5m2Dense {
 // --------------------------------------------------------------- K1 dense
 
 // One resident wave of CTAs; the code table is built once per CTA.  Tiles
-// are handed out one at a time from a counter in the workspace header (in
-// increasing order across the GPU), so CTAs that run faster take more tiles:
-// with a static split, CTAs of equal work finished up to three times apart.
-// Thread 0 draws the id of the tile two iterations ahead while the CTA works
-// on the current one; one CTA barrier per tile publishes it.  The input of
+// are handed out one at a time from counters in the workspace header, so CTAs
+// that run faster take more tiles: with a static split, CTAs of equal work
+// finished up to three times apart.  There are F::kStripes counters, each in
+// its own L2 line, stripe s handing out tiles s, s + kStripes, ... in
+// increasing order; a CTA draws from its home stripe and moves on to the next
+// when one runs dry.  Thread 0 draws the id of the tile two iterations ahead
+// while the CTA works on the current one; one CTA barrier per tile publishes
+// it.  The input of
 // full tiles comes through a per-thread ring of kDenseStages shared-memory
 // slots filled by cp.async: while a thread works on one tile, its copies of
 // the next kDenseStages - 1 tiles are in flight, with no registers held for
 // them.  A slot is refilled only after the values read from it have been used
 // by the tile's stores.
 constexpr int kDenseStages = 2;
+constexpr uint32_t kNoTile = 0xFFFFFFFFu;  // drawn once every stripe is dry
 
 template <class F>
 constexpr size_t dense_smem_bytes() {
@@ -566,17 +577,39 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
     static_assert(kDenseStages == 2, "two tile ids ahead");
     extern __shared__ uint4 ring[];  // [S][L][kThreads]
     __shared__ typename F::Tables tables;
-    __shared__ uint32_t s_grab[3];   // tile ids drawn by thread 0: [0..1] alternate, [2] the first pair
+    __shared__ uint32_t s_grab[4];   // tile ids drawn by thread 0: [0..1] alternate, [2..3] the first two
     __shared__ uint32_t s_tot[2];    // the tile's escape count, summed over the warps (alternate)
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
+    // Thread 0's draws with several stripes: from its home stripe, then from
+    // the next ones as they run dry; kNoTile once every stripe is dry (so no
+    // tile follows it).  With one (or p.striped false), the counter hands out
+    // tiles in order and the first draw takes two.
+    uint32_t tries = 0;
+    constexpr uint32_t NS = F::kStripes;
+    static_assert(NS >= 1 && NS <= kDenseStripes, "stripe counters in the header");
+    auto draw = [&]() -> uint32_t {
+        while (tries < NS) {
+            const uint32_t st = (blockIdx.x + tries) % NS;
+            const uint32_t t = st + NS * atomicAdd(&hdr->dense_stripe[st][0], 1u);
+            if (t < a.num_tiles) return t;
+            tries++;
+        }
+        return kNoTile;
+    };
     if (threadIdx.x == 0) {
-        s_grab[2] = atomicAdd(&hdr->dense_next, (uint32_t)S);
+        if (NS == 1 || !p.striped) {
+            s_grab[2] = atomicAdd(&hdr->dense_next, 2u);
+            s_grab[3] = s_grab[2] + 1;
+        } else {
+            s_grab[2] = draw();
+            s_grab[3] = draw();
+        }
         s_tot[0] = s_tot[1] = 0;
     }
     {
         uint32_t cbw[4];
         codebook_words(a.dcb, a.cbw, cbw);
-        F::build_tables(tables, cbw);  // ends with a CTA barrier: s_grab[2] is visible
+        F::build_tables(tables, cbw);  // ends with a CTA barrier: s_grab[2..3] are visible
     }
     // With F::kKeepLists, counts and list entries stay in L2 for the prefix and
     // placement passes while the tensor streams through.
@@ -591,13 +624,16 @@ __global__ void __launch_bounds__(kThreads, F::kMinBlocks) dense_kernel(const En
         }
         cp_async_commit();  // one group per tile, empty for a tile not staged
     };
-    uint32_t tile = s_grab[2], next = tile + 1;
+    uint32_t tile = s_grab[2], next = s_grab[3];
     fill(tile, 0);
     fill(next, 1);
     int slot = 0;
     uint32_t it = 0;
     for (; tile < a.num_tiles; it++) {
-        if (threadIdx.x == 0) s_grab[it & 1] = atomicAdd(&hdr->dense_next, 1u);  // two ahead
+        if (threadIdx.x == 0) {  // two ahead
+            if (NS == 1 || !p.striped) s_grab[it & 1] = atomicAdd(&hdr->dense_next, 1u);
+            else s_grab[it & 1] = draw();
+        }
         const uint32_t t0 = tile * (uint32_t)kTileElems;
         typename F::Keep kp;
         const uint8_t* in;  // the tile's input, from which the escapes are read
@@ -716,22 +752,40 @@ __device__ __forceinline__ uint32_t offset_in_block(uint32_t before, uint32_t ex
 // adding up to the superblocks show a workspace that started consistent.  (A
 // launch of its own: electing the last placement CTA cost every CTA a fence
 // and a returning atomic while it held its SM slot.)
+constexpr int kFinishThreads = 1024;
+constexpr int kFinishWarps = kFinishThreads / 32;
+constexpr uint32_t kMaxBlocks = kMaxSupers * (kSuperTiles / kBlockTiles);  // 8192
+
 template <class F>
-__global__ void __launch_bounds__(kThreads) finish_kernel(const EncodeArgs a, const MultiPtrs p) {
-    __shared__ uint32_t s_part[3][kWarps];
+__global__ void __launch_bounds__(kFinishThreads) finish_kernel(const EncodeArgs a, const MultiPtrs p) {
+    static_assert(kMaxBlocks % kFinishThreads == 0 && kMaxSupers <= kFinishThreads, "whole rounds");
+    constexpr int kPer = kMaxBlocks / kFinishThreads;
+    __shared__ uint32_t s_part[3][kFinishWarps];
     WsHeader* hdr = reinterpret_cast<WsHeader*>(a.ws);
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t e_sup = 0, e_blk = 0, t_blk = 0;
-    for (uint32_t i = threadIdx.x; i < p.nsupers; i += kThreads) {
-        e_sup += __ldcg(p.sup + i);
-        p.sup[i] = 0;
+    // Every count is loaded before any is used or zeroed, and thread 0's
+    // header words and device codebook with them (one memory round trip).
+    uint32_t dense_done = 0, status = 0, cbw[4] = {0, 0, 0, 0};
+    if (threadIdx.x == 0) {
+        dense_done = __ldcg(&hdr->dense_done);
+        status = __ldcg(&hdr->status);
+        if (a.dcb) codebook_words(a.dcb, a.cbw, cbw);
     }
-    for (uint32_t i = threadIdx.x; i < p.nblocks; i += kThreads) {
-        const uint32_t v = __ldcg(p.blk + i);
-        e_blk += v & kBlkEscMask;
-        t_blk += v >> kBlkCountShift;
-        p.blk[i] = 0;
+    uint32_t vb[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; k++) {
+        const uint32_t i = threadIdx.x + k * kFinishThreads;
+        vb[k] = i < p.nblocks ? __ldcg(p.blk + i) : 0u;
     }
+    uint32_t e_sup = threadIdx.x < p.nsupers ? __ldcg(p.sup + threadIdx.x) : 0u, e_blk = 0, t_blk = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; k++) {
+        e_blk += vb[k] & kBlkEscMask;
+        t_blk += vb[k] >> kBlkCountShift;
+        const uint32_t i = threadIdx.x + k * kFinishThreads;
+        if (i < p.nblocks) p.blk[i] = 0;
+    }
+    if (threadIdx.x < p.nsupers) p.sup[threadIdx.x] = 0;
 #pragma unroll
     for (int d = 16; d; d >>= 1) {
         e_sup += __shfl_xor_sync(0xFFFFFFFFu, e_sup, d);
@@ -747,24 +801,23 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const EncodeArgs a, co
     if (threadIdx.x == 0) {
         uint32_t total = 0, blocks = 0, counted = 0;
 #pragma unroll
-        for (int w = 0; w < kWarps; w++) {
+        for (int w = 0; w < kFinishWarps; w++) {
             total += s_part[0][w];
             blocks += s_part[1][w];
             counted += s_part[2][w];
         }
         a.chunk_off[a.nchunks] = total;
         hdr->last_escapes = total;
-        if ((uint64_t)total > a.esc_capacity) atomicOr(&hdr->status, kStatusOverflow);
-        if (a.dcb) {  // a codebook from device memory is checked here, once per encode
-            uint32_t cbw[4];
-            codebook_words(a.dcb, a.cbw, cbw);
-            if (!codebook_valid(cbw, F::kExpMask)) atomicOr(&hdr->status, kStatusBadCodebook);
-        }
-        if (atomicAdd(&hdr->dense_done, 0u) != a.num_tiles || counted != a.num_tiles ||
-            blocks != total)
-            atomicOr(&hdr->status, kStatusBadWorkspace);
-        hdr->last_status = atomicExch(&hdr->status, 0u);
+        if ((uint64_t)total > a.esc_capacity) status |= kStatusOverflow;
+        // A codebook from device memory is checked here, once per encode.
+        if (a.dcb && !codebook_valid(cbw, F::kExpMask)) status |= kStatusBadCodebook;
+        if (dense_done != a.num_tiles || counted != a.num_tiles || blocks != total)
+            status |= kStatusBadWorkspace;
+        hdr->last_status = status;
+        hdr->status = 0;
         hdr->done = 0;
+#pragma unroll
+        for (uint32_t st = 0; st < kDenseStripes; st++) hdr->dense_stripe[st][0] = 0;
         hdr->dense_next = 0;
         hdr->dense_done = 0;
         __threadfence();
@@ -1057,6 +1110,9 @@ cudaError_t launch_passes(const EncodeArgs& a, cudaStream_t s) {
     cudaError_t e = launch_wave<dense_kernel<F>>(kThreads, smem, wv);
     if (e != cudaSuccess) return e;
     const uint64_t wave = wv.ctas();
+    // Stripes pay off once every CTA takes many tiles; with few, the draws
+    // that find stripes dry at the end cost more than they save.
+    p.striped = F::kStripes > 1 && tiles >= 64 * wave;
     dense_kernel<F><<<(uint32_t)(tiles < wave ? tiles : wave), kThreads, smem, s>>>(a, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1072,7 +1128,7 @@ cudaError_t launch_passes(const EncodeArgs& a, cudaStream_t s) {
         place_kernel<F, 1><<<(tiles + kTilesPerRound - 1) / kTilesPerRound, kThreads, 0, s>>>(a, p, tiles);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    finish_kernel<F><<<1, kThreads, 0, s>>>(a, p);
+    finish_kernel<F><<<1, kFinishThreads, 0, s>>>(a, p);
     return cudaGetLastError();
 }
 
