@@ -283,6 +283,18 @@ __device__ __forceinline__ uint16_t ld_last2(const void* p) {
     asm volatile("ld.global.lu.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
+__device__ __forceinline__ uint2 ld_last8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.lu.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_last16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.lu.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 // cp_async16 with an L2 cache policy for the global read.
 __device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t pol) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),

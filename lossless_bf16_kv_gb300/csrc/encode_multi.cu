@@ -119,10 +119,14 @@ struct Bf16Dense {
     static constexpr int kSegs = 32;
     static constexpr int kSegLen = 256;
     static constexpr int kOffBits = 8;
-    static constexpr int kPlaceRounds = 4;  // placement: tiles per warp, one per round
-    static constexpr int kPreload = 4;      // placement: entries per segment loaded ahead
-    // Counts and lists stored plainly: evict-last stores measured 3% slower here.
-    static constexpr bool kKeepLists = false;
+    static constexpr int kPlaceRounds = 2;  // placement: rounds of four tiles per warp
+    static constexpr int kPreload = 4;      // (placement by segment: entries loaded ahead)
+    static constexpr bool kListPlace = true;  // placement with a lane per warp list
+    // Counts and lists stored evict-last, so that placement finds them in L2
+    // (with its 8- and 16-byte loads of them: 1.151 -> 1.144 ms per encode at
+    // 2^31 elements; with a lane per segment it had made the dense pass 3%
+    // slower).
+    static constexpr bool kKeepLists = true;
     static constexpr uint32_t kExpMask = 0xFFu;
     // Four tile counters, each hit by a quarter of the CTAs' draws (one
     // counter: 1.164 against 1.158 ms at 2^31 elements).
@@ -362,6 +366,7 @@ struct E5m2Dense {
     static constexpr int kOffBits = 10;
     static constexpr int kPlaceRounds = 2;  // placement: rounds of four tiles per warp
     static constexpr int kPreload = 8;      // placement: entries per segment loaded ahead
+    static constexpr bool kListPlace = false;  // a lane per segment (the segment is the warp's)
     // Counts and lists stored evict-last, so that placement finds them in L2.
     static constexpr bool kKeepLists = true;
     static constexpr uint32_t kExpMask = 0x1Fu;
@@ -1092,6 +1097,199 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
     }
 }
 
+// BF16 placement with a lane per warp list: in round r, lanes 8t..8t+7 take
+// tile tile0 + 4r + t and lane 8t + w the list the dense pass's warp w wrote,
+// which holds its four segments (w + 8k, elements 2048k + 256w .. + 255 of
+// the tile, k = 0..3) in order k.  The lane's four counts are one 8-byte
+// load; a scan of the counts packed two to a word (16-bit fields: a tile's
+// total per k is at most 8 x 256) over the tile's eight lanes gives each
+// segment's offset in the tile, the element order being k-major.  The lane
+// then walks its list's entries (the first eight from one 16-byte load).
+// Per tile this issues a fraction of the instructions of a lane per segment
+// (32 segments, each with its own scans and loads).
+__device__ __forceinline__ uint32_t pick4(uint32_t k, uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3) {
+    return k == 0 ? a0 : k == 1 ? a1 : k == 2 ? a2 : a3;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 4) place_lists_kernel(const EncodeArgs a,
+                                                                  const MultiPtrs p,
+                                                                  uint32_t num_tiles) {
+    using F = Bf16Dense;
+    constexpr uint32_t TPW = 4, G = 8;  // tiles per round, lanes (lists) per tile
+    constexpr uint32_t kOffMask = (1u << F::kOffBits) - 1u;
+    static_assert(G == kWarps && F::kSegLen * kWarps * 4 == kTileElems, "four segments per list");
+    static_assert(kBlockTiles % (TPW * R) == 0, "a warp's tiles lie in one block");
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ uint8_t isesc_all[kWarps][256];  // per warp: 1 for an exponent outside the codebook
+    uint8_t* isesc = isesc_all[warp];
+    const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW * R;
+    if (tile0 >= num_tiles) return;  // warp-uniform
+    const uint32_t sub = lane / G, w = lane % G;
+    auto tile_of = [&](int r) { return tile0 + (uint32_t)r * TPW + sub; };
+    auto list_of = [&](int r) {
+        return p.seg_ent + (size_t)tile_of(r) * kEntries + w * (uint32_t)kWarpCap;
+    };
+
+    // Round trip 1: every round's counts and the block's offsets.
+    uint2 c4[R];
+    uint32_t toff[R];
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        const uint32_t tile = tile_of(r);
+        c4[r] = tile < num_tiles ? ld_last8(p.seg_cnt + (size_t)tile * kSegsMax + 4 * w)
+                                 : make_uint2(0u, 0u);
+    }
+    {
+        uint32_t before, ex_lo, ex_hi;
+        block_offsets(p, tile0, num_tiles, before, ex_lo, ex_hi);
+        const uint32_t b0 = tile0 / kBlockTiles * kBlockTiles;
+#pragma unroll
+        for (int r = 0; r < R; r++) toff[r] = offset_in_block(before, ex_lo, ex_hi, tile_of(r) - b0);
+    }
+    // Round trip 2: the first eight entries of every non-empty list.
+    uint4 pre[R];
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        const bool any = (c4[r].x | c4[r].y) != 0u;
+        pre[r] = any ? ld_last16(list_of(r)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    const bool seg_in_chunk = a.cdiv.d % (uint32_t)F::kSegLen == 0;
+    bool table = false;
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+        const uint32_t tile = tile_of(r);
+        const bool valid = tile < num_tiles;
+        // Segment offsets in the tile: exclusive over the lower lists for the
+        // same k, plus the tile's totals of the lower k.
+        uint32_t i0 = c4[r].x, i1 = c4[r].y;
+#pragma unroll
+        for (uint32_t d = 1; d < G; d <<= 1) {
+            const uint32_t u0 = __shfl_up_sync(0xFFFFFFFFu, i0, d, G);
+            const uint32_t u1 = __shfl_up_sync(0xFFFFFFFFu, i1, d, G);
+            if (w >= d) {
+                i0 += u0;
+                i1 += u1;
+            }
+        }
+        const uint32_t T0 = __shfl_sync(0xFFFFFFFFu, i0, G - 1, G);
+        const uint32_t T1 = __shfl_sync(0xFFFFFFFFu, i1, G - 1, G);
+        const uint32_t e0 = i0 - c4[r].x, e1 = i1 - c4[r].y;
+        const uint32_t t0 = T0 & 0xFFFFu, t01 = t0 + (T0 >> 16), t012 = t01 + (T1 & 0xFFFFu);
+        const uint32_t off0 = e0 & 0xFFFFu, off1 = t0 + (e0 >> 16);
+        const uint32_t off2 = t01 + (e1 & 0xFFFFu), off3 = t012 + (e1 >> 16);
+        const uint32_t c0 = c4[r].x & 0xFFFFu, c1 = c4[r].x >> 16;
+        const uint32_t c2 = c4[r].y & 0xFFFFu, c3 = c4[r].y >> 16;
+        const uint32_t S1 = c0, S2 = c0 + c1, S3 = S2 + c2, tot = S3 + c3;
+        // Segments whose entries did not all fit in the list (rebuilt below).
+        const uint32_t ovf = (S1 > (uint32_t)kWarpCap ? 1u : 0u) | (S2 > (uint32_t)kWarpCap ? 2u : 0u) |
+                             (S3 > (uint32_t)kWarpCap ? 4u : 0u) | (tot > (uint32_t)kWarpCap ? 8u : 0u);
+        const uint32_t ovk = ovf & ((c0 ? 1u : 0u) | (c1 ? 2u : 0u) | (c2 ? 4u : 0u) | (c3 ? 8u : 0u));
+        const uint32_t t0e = tile * (uint32_t)kTileElems;
+        const uint32_t r0 = valid ? t0e - chunk_quot32(a.cdiv, t0e) * a.cdiv.d : 0u;
+        const uint32_t nl = valid ? (tot < (uint32_t)kWarpCap ? tot : (uint32_t)kWarpCap) : 0u;
+        const uint16_t* es = list_of(r);
+        for (uint32_t q = 0; q < nl; q++) {
+            const uint32_t k = (q >= S1 ? 1u : 0u) + (q >= S2 ? 1u : 0u) + (q >= S3 ? 1u : 0u);
+            if ((ovk >> k) & 1u) continue;  // rebuilt from the input
+            uint32_t e;
+            if (q < 8) {
+                const uint32_t v = pick4(q >> 1, pre[r].x, pre[r].y, pre[r].z, pre[r].w);
+                e = (v >> (16 * (q & 1u))) & 0xFFFFu;
+            } else {
+                e = ld_last2(es + q);
+            }
+            const uint32_t g = toff[r] + pick4(k, off0, off1, off2, off3) + q - pick4(k, 0u, S1, S2, S3);
+            const uint32_t x = r0 + 2048u * k + (uint32_t)F::kSegLen * w + (e & kOffMask);
+            put_escape(a, g, x - chunk_quot(a.cdiv, x) * a.cdiv.d, e >> F::kOffBits);
+        }
+        // Overflowed segments, rebuilt by the whole warp one at a time.
+        for (uint32_t ov = __ballot_sync(0xFFFFFFFFu, ovk != 0); ov; ov &= ov - 1) {
+            const uint32_t l = __ffs(ov) - 1;
+            const uint32_t lk = __shfl_sync(0xFFFFFFFFu, ovk, l);
+            const uint32_t lo0 = __shfl_sync(0xFFFFFFFFu, toff[r] + off0, l);
+            const uint32_t lo1 = __shfl_sync(0xFFFFFFFFu, toff[r] + off1, l);
+            const uint32_t lo2 = __shfl_sync(0xFFFFFFFFu, toff[r] + off2, l);
+            const uint32_t lo3 = __shfl_sync(0xFFFFFFFFu, toff[r] + off3, l);
+            if (!table) {  // warp-uniform
+                uint32_t cbw[4];
+                codebook_words(a.dcb, a.cbw, cbw);
+#pragma unroll
+                for (uint32_t ee = lane; ee < 256; ee += 32) isesc[ee] = !in_codebook(cbw, ee);
+                __syncwarp();
+                table = true;
+            }
+            for (uint32_t m = lk; m; m &= m - 1) {
+                const uint32_t k = __ffs(m) - 1;
+                rebuild_segment<F>(a, tile0 + (uint32_t)r * TPW + l / G, (l % G) + 8 * k,
+                                   pick4(k, lo0, lo1, lo2, lo3), isesc);
+            }
+        }
+        // chunk_off at the chunk starts of the tile.  When the chunk size is a
+        // multiple of the segment length every chunk start is a segment start
+        // (tiles and segments start at multiples of it), written by the lane
+        // of that segment's list.
+        if (seg_in_chunk) {
+            if (!valid) continue;
+            const uint32_t len = a.n - t0e < (uint32_t)kTileElems ? a.n - t0e : (uint32_t)kTileElems;
+            const uint32_t q0 = chunk_quot32(a.cdiv, t0e);
+#pragma unroll
+            for (uint32_t k = 0; k < 4; k++) {
+                const uint32_t ps = 2048u * k + (uint32_t)F::kSegLen * w;  // the segment's start
+                const uint32_t x = r0 + ps, qx = chunk_quot(a.cdiv, x);  // x < d + kTileElems
+                if (ps < len && x == qx * a.cdiv.d)
+                    a.chunk_off[q0 + qx] = toff[r] + pick4(k, off0, off1, off2, off3);
+            }
+            continue;
+        }
+        // Other chunk sizes: the rank of each chunk start from the offset of
+        // the segment holding it and that segment's entries before it.
+        for (uint32_t t = 0; t < TPW; t++) {
+            const uint32_t tl = tile0 + (uint32_t)r * TPW + t;
+            if (tl >= num_tiles) break;  // warp-uniform
+            const uint32_t u0 = tl * (uint32_t)kTileElems;
+            const uint32_t ulen = a.n - u0 < (uint32_t)kTileElems ? a.n - u0 : (uint32_t)kTileElems;
+            const uint32_t uq0 = chunk_quot32(a.cdiv, u0), ur0 = u0 - uq0 * a.cdiv.d;
+            const uint16_t* uent = p.seg_ent + (size_t)tl * kEntries;
+            const uint32_t qa = ur0 ? 1u : 0u, qb = chunk_quot(a.cdiv, ur0 + ulen - 1);
+            for (uint32_t b0 = qa; b0 <= qb; b0 += 32) {
+                const uint32_t q = b0 + lane;
+                const bool ok = q <= qb;
+                const uint32_t bl = ok ? q * a.cdiv.d - ur0 : 0u;  // tile-local chunk start
+                const uint32_t sg = bl / (uint32_t)F::kSegLen, sw = sg & 7u, sk = sg >> 3;
+                const uint32_t src = t * G + sw;  // the lane holding that segment's list
+                const uint32_t so0 = __shfl_sync(0xFFFFFFFFu, toff[r] + off0, src);
+                const uint32_t so1 = __shfl_sync(0xFFFFFFFFu, toff[r] + off1, src);
+                const uint32_t so2 = __shfl_sync(0xFFFFFFFFu, toff[r] + off2, src);
+                const uint32_t so3 = __shfl_sync(0xFFFFFFFFu, toff[r] + off3, src);
+                const uint32_t sS1 = __shfl_sync(0xFFFFFFFFu, S1, src);
+                const uint32_t sS2 = __shfl_sync(0xFFFFFFFFu, S2, src);
+                const uint32_t sS3 = __shfl_sync(0xFFFFFFFFu, S3, src);
+                const uint32_t stot = __shfl_sync(0xFFFFFFFFu, tot, src);
+                if (ok) {
+                    const uint32_t base = pick4(sk, 0u, sS1, sS2, sS3);
+                    const uint32_t end = pick4(sk, sS1, sS2, sS3, stot);
+                    const uint32_t lim = bl - sg * (uint32_t)F::kSegLen;
+                    uint32_t rank = 0;
+                    if (lim == 0) {
+                    } else if (end <= (uint32_t)kWarpCap) {
+                        const uint16_t* e = uent + sw * (uint32_t)kWarpCap;
+                        for (uint32_t q2 = base; q2 < end; q2++) rank += (e[q2] & kOffMask) < lim;
+                    } else {
+                        uint32_t cbw[4];
+                        codebook_words(a.dcb, a.cbw, cbw);
+                        for (uint32_t l2 = sg * (uint32_t)F::kSegLen; l2 < bl; l2++)
+                            rank += !in_codebook(cbw, F::exponent_at(a, u0 + l2));
+                    }
+                    a.chunk_off[uq0 + q] = pick4(sk, so0, so1, so2, so3) + rank;
+                }
+            }
+        }
+    }
+}
+
 template <class F>
 cudaError_t launch_passes(const EncodeArgs& a, cudaStream_t s) {
     const MultiLayout L = multi_layout(a.n);
@@ -1122,10 +1320,18 @@ cudaError_t launch_passes(const EncodeArgs& a, cudaStream_t s) {
     constexpr uint32_t kTilesPerRound = kWarps * (32 / F::kSegs);  // per CTA
     const uint64_t two_waves = 2ull * (uint64_t)(wv.sms > 0 ? wv.sms : 1) * 4;  // 4 CTAs per SM
     const uint32_t wide = kTilesPerRound * F::kPlaceRounds;
-    if ((tiles + wide - 1) / wide >= two_waves)
+    if constexpr (F::kListPlace) {  // a lane per warp list, four tiles per warp and round
+        constexpr uint32_t kListRound = kWarps * 4;  // tiles per CTA and round
+        const uint32_t wide2 = kListRound * F::kPlaceRounds;
+        if ((tiles + wide2 - 1) / wide2 >= two_waves)
+            place_lists_kernel<F::kPlaceRounds><<<(tiles + wide2 - 1) / wide2, kThreads, 0, s>>>(a, p, tiles);
+        else
+            place_lists_kernel<1><<<(tiles + kListRound - 1) / kListRound, kThreads, 0, s>>>(a, p, tiles);
+    } else if ((tiles + wide - 1) / wide >= two_waves) {
         place_kernel<F, F::kPlaceRounds><<<(tiles + wide - 1) / wide, kThreads, 0, s>>>(a, p, tiles);
-    else
+    } else {
         place_kernel<F, 1><<<(tiles + kTilesPerRound - 1) / kTilesPerRound, kThreads, 0, s>>>(a, p, tiles);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     finish_kernel<F><<<1, kFinishThreads, 0, s>>>(a, p);
