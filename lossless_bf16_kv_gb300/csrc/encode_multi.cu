@@ -9,21 +9,23 @@
 // The only cross-tile dependency of the format is the escape stream's order
 // (chunk, then position) and its offsets.  Here it is taken out of the
 // streaming pass:
-//   dense   one resident wave of CTAs drawing 8192-element tiles from a
-//           counter: input staged through a per-thread cp.async ring, field
-//           split, code lookup in shared-memory word tables, dense code and
-//           sign+mantissa stores.  Each warp ranks the escapes of its
-//           segments (ballots when no group holds two escapes, else one
-//           shuffle scan) and stores the segments' counts and its first 32
-//           escapes, as one list in element order within each segment, in the
-//           workspace; the tile's count goes to the tile's, its block's and
-//           its superblock's counters.
-//   place   a warp per tile (BF16) or four (E5M2): the tile offsets from the
-//           block and superblock counters (no scan pass, no waits), segment
-//           offsets by shuffle scan, escapes copied to their final places,
-//           chunk offsets at chunk starts.  A segment whose escapes do not all
-//           fit in its warp's list is rebuilt from the input by the whole
-//           warp.
+//   dense   one resident wave of CTAs drawing 8192-element tiles from one
+//           counter (four for large BF16 tensors): input staged through a
+//           per-thread cp.async ring, field split, code lookup in shared-
+//           memory word tables, dense code and sign+mantissa stores.  Each
+//           warp ranks the escapes of its segments (ballots when no group
+//           holds two escapes, else one shuffle scan) and stores the
+//           segments' counts and its first 32 escapes, as one list in element
+//           order within each segment, in the workspace; the tile's count
+//           goes to the tile's and its block's counters, a completed block's
+//           to its superblock's.
+//   place   four tiles per warp and round, a lane per warp list (BF16: eight
+//           lists of four segments per tile) or per segment (E5M2: eight per
+//           tile): the tile offsets from the block and superblock counters
+//           (no scan pass, no waits), segment offsets by shuffle scans,
+//           escapes copied to their final places, chunk offsets at chunk
+//           starts.  A segment whose escapes do not all fit in its warp's
+//           list is rebuilt from the input by the whole warp.
 //   finish  one CTA: E, chunk_off[C], the call's status and checks; re-arms
 //           the counters.
 // Segments: BF16 -- the 256 consecutive elements warp w covers with its group
@@ -41,7 +43,7 @@
 namespace splitzip {
 namespace {
 
-constexpr int kTileElems = 8192;     // elements per tile (K1 CTA / K3 warp)
+constexpr int kTileElems = 8192;     // elements per tile (dense pass: a CTA per tile at a time)
 constexpr int kSegsMax = 32;         // segment slots per tile in the workspace
 constexpr int kEntries = 256;        // escape entries per tile in the workspace
 constexpr int kWarpCap = kEntries / kWarps;  // 32: entries of one warp's escape list
@@ -120,7 +122,6 @@ struct Bf16Dense {
     static constexpr int kSegLen = 256;
     static constexpr int kOffBits = 8;
     static constexpr int kPlaceRounds = 2;  // placement: rounds of four tiles per warp
-    static constexpr int kPreload = 4;      // (placement by segment: entries loaded ahead)
     static constexpr bool kListPlace = true;  // placement with a lane per warp list
     // Counts and lists stored evict-last, so that placement finds them in L2
     // (with its 8- and 16-byte loads of them: 1.151 -> 1.144 ms per encode at
@@ -146,7 +147,6 @@ struct Bf16Dense {
     // Segment 8k + w (element order: group k of warp w) is kept at workspace
     // slot 4w + k, so that a warp's four counts are one 8-byte store.
     static __device__ __forceinline__ uint32_t slot(int k) { return (threadIdx.x >> 5) * 4 + k; }
-    static __device__ __forceinline__ uint32_t storage(uint32_t s) { return (s & 7u) * 4 + (s >> 3); }
     static __device__ __forceinline__ void build_tables(Tables& tb, const uint32_t (&cbw)[4]) {
         const uint32_t tid = threadIdx.x;
 #pragma unroll
@@ -338,19 +338,7 @@ struct Bf16Dense {
         }
     }
 
-    // Warp list of segment s (element order 8k + w) and, from the counts held
-    // by the lanes of its tile (lane base + s holds segment s; all lanes call
-    // it), the entries of the warp's lower groups that precede it there.
-    static __device__ __forceinline__ uint32_t seg_list(uint32_t s) { return s & 7u; }
-    static __device__ __forceinline__ uint32_t seg_base(uint32_t s, uint32_t cnt, uint32_t lbase) {
-        const uint32_t w = s & 7u, k = s >> 3;
-        const uint32_t n0 = __shfl_sync(0xFFFFFFFFu, cnt, lbase + w);
-        const uint32_t n1 = __shfl_sync(0xFFFFFFFFu, cnt, lbase + 8 + w);
-        const uint32_t n2 = __shfl_sync(0xFFFFFFFFu, cnt, lbase + 16 + w);
-        return (k > 0 ? n0 : 0u) + (k > 1 ? n1 : 0u) + (k > 2 ? n2 : 0u);
-    }
-
-    // Exponent of element i of the input (K3's rebuild of a full segment).
+    // Exponent of element i of the input (placement's chunk ranks).
     static __device__ __forceinline__ uint32_t exponent_at(const EncodeArgs& a, uint32_t i) {
         return (reinterpret_cast<const uint16_t*>(a.x)[i] >> 7) & 0xFFu;
     }
@@ -551,7 +539,7 @@ struct E5m2Dense {
     }
 };
 
-// --------------------------------------------------------------- K1 dense
+// ------------------------------------------------------------ dense pass
 
 // One resident wave of CTAs; the code table is built once per CTA.  Tiles
 // are handed out one at a time from counters in the workspace header, so CTAs
@@ -829,7 +817,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const EncodeArgs
     }
 }
 
-// --------------------------------------------------------------- K3 place
+// ------------------------------------------------------------- placement
 
 __device__ __forceinline__ void put_escape(const EncodeArgs& a, uint32_t g, uint32_t pos,
                                            uint32_t e) {
@@ -916,8 +904,9 @@ __device__ __forceinline__ void rebuild_segment(const EncodeArgs& a, uint32_t ti
     }
 }
 
-// A warp places the escapes of F::kPlaceRounds x 32 / kSegs consecutive tiles
-// (BF16: 4 x 1, E5M2: 2 x 4): in round r lane l takes segment l mod kSegs
+// Placement with a lane per segment (E5M2, whose segment is a warp's whole
+// list).  A warp places the escapes of F::kPlaceRounds x 32 / kSegs
+// consecutive tiles (2 x 4): in round r lane l takes segment l mod kSegs
 // (element order) of tile tile0 + r * 32 / kSegs + l / kSegs.  Every round's
 // tile offset and counts are loaded before any is used, and every round's
 // first F::kPreload entries before any escape is stored (loads cannot pass
