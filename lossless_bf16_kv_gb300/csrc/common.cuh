@@ -277,6 +277,15 @@ __device__ __forceinline__ void st_policy8(void* p, uint2 v, uint64_t pol) {
                  "r"(v.y), "l"(pol)
                  : "memory");
 }
+// Programmatic dependent launch: a grid lets the launch that depends on it
+// start early, and that launch waits until this grid has completed and its
+// memory operations are visible before it goes past wait_prerequisite_grid.
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prerequisite_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 // Loads of data read for the last time (evict-first in L2).
 __device__ __forceinline__ uint16_t ld_last2(const void* p) {
     uint16_t v;

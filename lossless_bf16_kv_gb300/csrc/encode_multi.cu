@@ -775,6 +775,13 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const EncodeArgs
     for (int k = 0; k < kPer; k++) {
         e_blk += vb[k] & kBlkEscMask;
         t_blk += vb[k] >> kBlkCountShift;
+    }
+    // Placement reads the counters: zero them (and write the call's results)
+    // only once it has finished.  The loads above read what the dense pass
+    // wrote, complete before placement started.
+    wait_prerequisite_grid();
+#pragma unroll
+    for (int k = 0; k < kPer; k++) {
         const uint32_t i = threadIdx.x + k * kFinishThreads;
         if (i < p.nblocks) p.blk[i] = 0;
     }
@@ -923,6 +930,7 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
     __shared__ uint8_t isesc_all[kWarps][256];  // per warp: 1 for an exponent outside the codebook
     uint8_t* isesc = isesc_all[warp];
     const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW * R;
+    launch_dependents();             // the finishing launch may start (it waits for this grid)
     if (tile0 >= num_tiles) return;  // warp-uniform
     const uint32_t sub = lane / SEGS, sgl = lane % SEGS;  // this lane's tile and segment
     const uint32_t lbase = lane & ~(SEGS - 1);
@@ -1114,6 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 4) place_lists_kernel(const EncodeAr
     __shared__ uint8_t isesc_all[kWarps][256];  // per warp: 1 for an exponent outside the codebook
     uint8_t* isesc = isesc_all[warp];
     const uint32_t tile0 = (blockIdx.x * kWarps + warp) * TPW * R;
+    launch_dependents();             // the finishing launch may start (it waits for this grid)
     if (tile0 >= num_tiles) return;  // warp-uniform
     const uint32_t sub = lane / G, w = lane % G;
     auto tile_of = [&](int r) { return tile0 + (uint32_t)r * TPW + sub; };
@@ -1323,8 +1332,18 @@ cudaError_t launch_passes(const EncodeArgs& a, cudaStream_t s) {
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    finish_kernel<F><<<1, kFinishThreads, 0, s>>>(a, p);
-    return cudaGetLastError();
+    // A programmatic dependent launch: the finishing CTA loads and sums the
+    // counters while placement runs and waits for it only to write.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kFinishThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, finish_kernel<F>, a, p);
 }
 
 }  // namespace
