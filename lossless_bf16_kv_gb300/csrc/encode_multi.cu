@@ -973,13 +973,17 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
     auto entries = [&](int r) {
         return p.seg_ent + (size_t)tile_of(r) * kEntries + F::seg_list(sgl) * kWarpCap + sbase[r];
     };
+    // Every segment is a whole warp list, starting on a 16-byte boundary: its
+    // first eight entries are one 16-byte load.
+    static_assert(K == 8 && SEGS == kWarps, "a list per segment, eight entries preloaded");
     uint32_t ev[R][K];
 #pragma unroll
     for (int r = 0; r < R; r++) {
         const bool listed = sbase[r] + cnt[r] <= (uint32_t)kWarpCap;
-        const uint16_t* es = entries(r);
+        const uint4 v = listed && cnt[r] ? ld_last16(entries(r)) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int k = 0; k < K; k++) ev[r][k] = listed && (uint32_t)k < cnt[r] ? ld_last2(es + k) : 0u;
+        for (int k = 0; k < K; k++) ev[r][k] = (vw[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
     }
 
     // Escapes of segment sgl of each round's tile, in element order.  When the
