@@ -1115,12 +1115,19 @@ __device__ __forceinline__ uint32_t pick4(uint32_t k, uint32_t a0, uint32_t a1, 
     return k == 0 ? a0 : k == 1 ? a1 : k == 2 ? a2 : a3;
 }
 
-template <int R>
+//
+// TPW tiles per warp and round: four, or two for smaller tensors (lanes
+// 16..31 idle).  With four, a tensor of 2^26 elements leaves 13 warps per SM,
+// and with 60% escapes each rebuilt up to 128 overflowed segments one after
+// another (encode 0.37 ms against 0.245 with two and 0.225 with one); a tile
+// per warp made the KV layer 3 us slower (54 against 51 us).
+template <int R, uint32_t TPW>
 __global__ void __launch_bounds__(kThreads, 4) place_lists_kernel(const EncodeArgs a,
                                                                   const MultiPtrs p,
                                                                   uint32_t num_tiles) {
     using F = Bf16Dense;
-    constexpr uint32_t TPW = 4, G = 8;  // tiles per round, lanes (lists) per tile
+    constexpr uint32_t G = 8;  // lanes (lists) per tile
+    static_assert(TPW == 1 || TPW == 2 || TPW == 4, "one, two or four tiles per warp and round");
     constexpr uint32_t kOffMask = (1u << F::kOffBits) - 1u;
     static_assert(G == kWarps && F::kSegLen * kWarps * 4 == kTileElems, "four segments per list");
     static_assert(kBlockTiles % (TPW * R) == 0, "a warp's tiles lie in one block");
@@ -1132,7 +1139,8 @@ __global__ void __launch_bounds__(kThreads, 4) place_lists_kernel(const EncodeAr
     launch_dependents();             // the finishing launch may start (it waits for this grid)
     if (tile0 >= num_tiles) return;  // warp-uniform
     const uint32_t sub = lane / G, w = lane % G;
-    auto tile_of = [&](int r) { return tile0 + (uint32_t)r * TPW + sub; };
+    // The lane's tile; num_tiles (no tile) for an idle lane.
+    auto tile_of = [&](int r) { return sub < TPW ? tile0 + (uint32_t)r * TPW + sub : num_tiles; };
     auto list_of = [&](int r) {
         return p.seg_ent + (size_t)tile_of(r) * kEntries + w * (uint32_t)kWarpCap;
     };
@@ -1194,11 +1202,13 @@ __global__ void __launch_bounds__(kThreads, 4) place_lists_kernel(const EncodeAr
         const uint32_t ovk = ovf & ((c0 ? 1u : 0u) | (c1 ? 2u : 0u) | (c2 ? 4u : 0u) | (c3 ? 8u : 0u));
         const uint32_t t0e = tile * (uint32_t)kTileElems;
         const uint32_t r0 = valid ? t0e - chunk_quot32(a.cdiv, t0e) * a.cdiv.d : 0u;
-        const uint32_t nl = valid ? (tot < (uint32_t)kWarpCap ? tot : (uint32_t)kWarpCap) : 0u;
+        // The listed segments are a prefix of the four (the ends S1, S2, S3,
+        // tot grow): walk the entries up to the end of the last one.
+        const uint32_t cap = (uint32_t)kWarpCap;
+        const uint32_t nl = !valid ? 0u : tot <= cap ? tot : S3 <= cap ? S3 : S2 <= cap ? S2 : S1 <= cap ? S1 : 0u;
         const uint16_t* es = list_of(r);
         for (uint32_t q = 0; q < nl; q++) {
             const uint32_t k = (q >= S1 ? 1u : 0u) + (q >= S2 ? 1u : 0u) + (q >= S3 ? 1u : 0u);
-            if ((ovk >> k) & 1u) continue;  // rebuilt from the input
             uint32_t e;
             if (q < 8) {
                 const uint32_t v = pick4(q >> 1, pre[r].x, pre[r].y, pre[r].z, pre[r].w);
@@ -1342,12 +1352,13 @@ cudaError_t launch_passes(const EncodeArgs& a, cudaStream_t s) {
         cfg.numAttrs = early ? 1 : 0;
         return cudaLaunchKernelEx(&cfg, kernel, a, p, tiles);
     };
-    if constexpr (F::kListPlace) {  // a lane per warp list, four tiles per warp and round
-        constexpr uint32_t kListRound = kWarps * 4;  // tiles per CTA and round
-        const uint32_t wide2 = kListRound * F::kPlaceRounds;
+    if constexpr (F::kListPlace) {  // a lane per warp list
+        // Four tiles per warp in kPlaceRounds rounds, or two tiles per warp
+        // when that would leave fewer than two waves of CTAs.
+        const uint32_t wide2 = kWarps * 4 * F::kPlaceRounds;  // tiles per CTA
         e = (tiles + wide2 - 1) / wide2 >= two_waves
-                ? launch(place_lists_kernel<F::kPlaceRounds>, (tiles + wide2 - 1) / wide2, kThreads)
-                : launch(place_lists_kernel<1>, (tiles + kListRound - 1) / kListRound, kThreads);
+                ? launch(place_lists_kernel<F::kPlaceRounds, 4>, (tiles + wide2 - 1) / wide2, kThreads)
+                : launch(place_lists_kernel<1, 2>, (tiles + 2 * kWarps - 1) / (2 * kWarps), kThreads);
     } else {
         e = (tiles + wide - 1) / wide >= two_waves
                 ? launch(place_kernel<F, F::kPlaceRounds>, (tiles + wide - 1) / wide, kThreads)
