@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # The encode call is three launches (dense pass, escape placement, a one-CTA
 # finish; the dense pass takes about 92% of the time), decode one.  The
 # roofline is taken per call: algorithmic bytes of the call over its time.
-KERNELS = {"encode": ("encode[dense_kernel+place_kernel+finish_kernel]<Bf16Dense>",
+KERNELS = {"encode": ("encode[dense_kernel+place_lists_kernel+finish_kernel]<Bf16Dense>",
                       "encode[dense_kernel+place_kernel+finish_kernel]<E5m2Dense>"),
            "decode": ("decode_kernel<Bf16Seg>", "decode_e5m2_kernel")}
 
