@@ -1101,7 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 4) place_kernel(const EncodeArgs a, 
 }
 
 // BF16 placement with a lane per warp list: in round r, lanes 8t..8t+7 take
-// tile tile0 + 4r + t and lane 8t + w the list the dense pass's warp w wrote,
+// tile tile0 + TPW r + t and lane 8t + w the list the dense pass's warp w wrote,
 // which holds its four segments (w + 8k, elements 2048k + 256w .. + 255 of
 // the tile, k = 0..3) in order k.  The lane's four counts are one 8-byte
 // load; a scan of the counts packed two to a word (16-bit fields: a tile's
@@ -1115,7 +1115,6 @@ __device__ __forceinline__ uint32_t pick4(uint32_t k, uint32_t a0, uint32_t a1, 
     return k == 0 ? a0 : k == 1 ? a1 : k == 2 ? a2 : a3;
 }
 
-//
 // TPW tiles per warp and round: four, or two for smaller tensors (lanes
 // 16..31 idle).  With four, a tensor of 2^26 elements leaves 13 warps per SM,
 // and with 60% escapes each rebuilt up to 128 overflowed segments one after
