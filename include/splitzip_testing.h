@@ -11,9 +11,9 @@
  * bounds and returns, leaving the CUDA context usable.  This entry point lets
  * a test make that wait run out on purpose, with a flag that keeps tile 0
  * from ever publishing, and a small poll limit so the test ends quickly.  (The
- * default three-launch encode has no waits: its tile offsets come from counters
- * the first launch completes before the second starts; the stall flag has no
- * effect on it.)  The method's pages have no counterpart: this entry point
+ * default three-launch encode has no spin-waits: its tile offsets come from
+ * counters the first launch completes before the second reads them; the stall
+ * flag has no effect on it.)  The method's pages have no counterpart: this entry point
  * exists only to exercise the error path.
  */
 #ifndef SPLITZIP_TESTING_H
