@@ -205,6 +205,41 @@ def test_concurrent_streams():
             assert np.array_equal(host_bits(y), host_bits(x))
 
 
+def test_concurrent_streams_with_a_large_bf16_encode():
+    """A BF16 tensor large enough that its dense pass draws tiles from four
+    counters (about 2^29 elements), encoded and decoded on one stream while
+    small tensors are encoded and decoded on two others (their placements
+    launched as dependents of their dense passes): every call's streams are
+    the oracle's."""
+    from lossless_bf16_kv_gb300 import splitzip as sz
+    fmts = ["bf16", "bf16", "e5m2"]
+    xs = [synth.kv_cache(16, 16400, seed=21, device=DEV).reshape(-1),
+          synth.kv_cache(1, 3000, seed=22, device=DEV).reshape(-1),
+          synth.kv_cache(1, 2500, seed=23, device=DEV, dtype=torch.float8_e5m2).reshape(-1)]
+    cbs = [gpu_calibrate(x)[0] for x in xs]
+    streams = [torch.cuda.Stream() for _ in xs]
+    wss = [sz.alloc_workspace(x.numel(), DEV) for x in xs]
+    outs = [sz.alloc_streams(x.numel(), 1024, f, x.numel() // 16, DEV) for x, f in zip(xs, fmts)]
+    ys = [torch.empty_like(x) for x in xs]
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for x, f, cb, st, ws, o, y in zip(xs, fmts, cbs, streams, wss, outs, ys):
+            with torch.cuda.stream(st):
+                sz.splitzip_encode(x, 1024, cb, o, ws, f, stream=st)
+                sz.splitzip_decode(o, x.numel(), 1024, cb, y, f, stream=st)
+        torch.cuda.synchronize()
+    for x, f, cb, st, ws, o, y in zip(xs, fmts, cbs, streams, wss, outs, ys):
+        status, E = sz.splitzip_encode_status(ws, st)
+        assert status == sz.OK
+        ref = oracle.encode(host_bits(x), 1024, np.asarray(cb, np.uint8), f)
+        got = {"codes": o["codes"].cpu().numpy(), "signman": o["signman"].cpu().numpy(),
+               "chunk_off": o["chunk_off"].cpu().numpy().view(np.uint32),
+               "esc_pos": o["esc_pos"][:E].cpu().numpy().view(np.uint16),
+               "esc_val": o["esc_val"][:E].cpu().numpy(), "n_escapes": E}
+        assert_streams_equal(got, ref, f"concurrent {f} n={x.numel()}")
+        assert np.array_equal(host_bits(y), host_bits(x))
+
+
 # ------------------------------------------- the single-launch engine
 
 @pytest.mark.parametrize("fmt", ["bf16", "e5m2"])
